@@ -1,0 +1,300 @@
+// Host side of the C ABI in include/memra.h: argument validation, the split
+// plan, shared-memory sizing and the kernel launches.  Nothing here allocates
+// device memory or synchronizes, except memra_read_status.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "decode_kernel.cuh"
+
+using namespace memra;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool k_format_ok(int f) { return f == MEMRA_KV_Q8_0 || f == MEMRA_KV_FP8_E4M3; }
+bool v_format_ok(int f) { return f == MEMRA_KV_Q5_1 || f == MEMRA_KV_Q4_0 || f == MEMRA_KV_FP8_E4M3; }
+
+int check_cache(const memra_kv_cache *c) {
+  if (!c) return MEMRA_ERR_INVALID_ARG;
+  if (!k_format_ok(c->k_fmt) || !v_format_ok(c->v_fmt)) return MEMRA_ERR_UNSUPPORTED;
+  if (c->page_size != MEMRA_PAGE_SIZE) return MEMRA_ERR_UNSUPPORTED;
+  if (c->head_dim != 128 && c->head_dim != 256) return MEMRA_ERR_UNSUPPORTED;
+  if (c->n_kv_heads < 1 || c->num_pages < 1) return MEMRA_ERR_INVALID_ARG;
+  if (!c->k_pool || !c->v_pool || !aligned16(c->k_pool) || !aligned16(c->v_pool)) return MEMRA_ERR_INVALID_ARG;
+  if (c->status && (reinterpret_cast<uintptr_t>(c->status) & 3u)) return MEMRA_ERR_INVALID_ARG;
+  if (c->k_fmt == MEMRA_KV_FP8_E4M3 && !(std::isfinite(c->k_scale) && c->k_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
+  if (c->v_fmt == MEMRA_KV_FP8_E4M3 && !(std::isfinite(c->v_scale) && c->v_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
+  // pools larger than 2^31 segments per head are fine (size_t offsets)
+  return MEMRA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MEMRA_OK : MEMRA_ERR_CUDA; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int nt, ngrp, qg, nsplit_max, num_stages;
+  size_t smem;
+};
+
+size_t merge_bytes(int D, int nt) {
+  const size_t rows_w = 8 * nt, nb = D / 32;
+  const size_t w = kConsumerWarps;
+  return (w * rows_w * D + 2 * w * rows_w + w * rows_w * nb) * 4;
+}
+
+// Row tiling and pipeline depth.  Rows (q_len x group) are cut into groups of
+// 8*nt rows per warp; the 4 consumer warps split into row groups x page lanes.
+int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan *pl) {
+  const int qg = q_len * group;
+  int nt, ngrp;
+  if (qg <= 8) {
+    nt = 1;
+    ngrp = 1;
+  } else if (D == 128) {
+    nt = 2;
+    ngrp = static_cast<int>(ceil_div(qg, 16));
+  } else {
+    nt = 1;
+    ngrp = static_cast<int>(ceil_div(qg, 8));
+  }
+  if (ngrp == 3) ngrp = 4;
+  if (ngrp > kConsumerWarps) return MEMRA_ERR_UNSUPPORTED;
+  const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
+  const size_t budget = 100 * 1024;
+  int ns = static_cast<int>(budget / stage);
+  if (ns > 16) ns = 16;
+  if (ns < 4) ns = 4;
+  size_t region = stage * ns;
+  const size_t mb = merge_bytes(D, nt);
+  if (mb > region) region = mb;
+  pl->nt = nt;
+  pl->ngrp = ngrp;
+  pl->qg = qg;
+  pl->nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
+  pl->num_stages = ns;
+  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(ns);
+  return MEMRA_OK;
+}
+
+size_t workspace_parts(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, int32_t max_seq_len,
+                       size_t *lse_offset) {
+  const size_t rows = static_cast<size_t>(batch) * q_len * n_heads;
+  const size_t ns = static_cast<size_t>(ceil_div(max_seq_len, kSplitTokens));
+  size_t o_bytes = rows * ns * head_dim * sizeof(float);
+  o_bytes = (o_bytes + 255) & ~static_cast<size_t>(255);
+  if (lse_offset) *lse_offset = o_bytes;
+  return o_bytes + rows * ns * sizeof(float);
+}
+
+struct DecodeArgs {
+  const memra_kv_cache *cache;
+  const void *q;
+  const int32_t *page_table;
+  int32_t max_pages_per_seq;
+  const int32_t *seq_lens;
+  int32_t max_seq_len, batch, q_len, n_heads, n_kv_heads, head_dim;
+  float sm_scale;
+  void *workspace;
+  size_t workspace_bytes;
+  void *out;
+};
+
+int check_decode(const DecodeArgs &a) {
+  int st = check_cache(a.cache);
+  if (st) return st;
+  if (a.batch < 0 || a.q_len < 1 || a.n_heads < 1 || a.max_seq_len < 0 || a.max_pages_per_seq < 0)
+    return MEMRA_ERR_INVALID_ARG;
+  if (a.n_kv_heads != a.cache->n_kv_heads || a.head_dim != a.cache->head_dim) return MEMRA_ERR_INVALID_ARG;
+  if (a.n_heads % a.n_kv_heads) return MEMRA_ERR_INVALID_ARG;
+  if (!std::isfinite(a.sm_scale)) return MEMRA_ERR_INVALID_ARG;
+  if (a.batch == 0) return MEMRA_OK;
+  if (!a.q || !a.page_table || !a.seq_lens || !a.out) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned16(a.q) || !aligned16(a.out) || (reinterpret_cast<uintptr_t>(a.page_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
+    return MEMRA_ERR_INVALID_ARG;
+  if (a.max_pages_per_seq < 1) return MEMRA_ERR_INVALID_ARG;
+  const size_t need = workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, nullptr);
+  if (a.workspace_bytes < need) return MEMRA_ERR_WORKSPACE;
+  if (need > 0 && (!a.workspace || !aligned16(a.workspace))) return MEMRA_ERR_INVALID_ARG;
+  return MEMRA_OK;
+}
+
+int run_partials(const DecodeArgs &a, cudaStream_t st) {
+  const memra_kv_cache &c = *a.cache;
+  Plan pl;
+  const int group = a.n_heads / a.n_kv_heads;
+  int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl);
+  if (rc) return rc;
+  if (pl.nsplit_max == 0) return MEMRA_OK;    // every sequence is empty; the combine writes zeros
+  size_t lse_off = 0;
+  workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, &lse_off);
+  DecodeParams p;
+  p.k_pool = static_cast<const uint8_t *>(c.k_pool);
+  p.v_pool = static_cast<const uint8_t *>(c.v_pool);
+  p.q = static_cast<const __half *>(a.q);
+  p.page_table = a.page_table;
+  p.seq_lens = a.seq_lens;
+  p.out = static_cast<__half *>(a.out);
+  p.o_part = static_cast<float *>(a.workspace);
+  p.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + lse_off);
+  p.status = c.status;
+  p.n_kv_heads = c.n_kv_heads;
+  p.num_pages = c.num_pages;
+  p.max_pages = a.max_pages_per_seq;
+  p.max_seq_len = a.max_seq_len;
+  p.q_len = a.q_len;
+  p.n_heads = a.n_heads;
+  p.group = group;
+  p.qg = pl.qg;
+  p.nsplit_max = pl.nsplit_max;
+  p.num_stages = pl.num_stages;
+  p.ngrp = pl.ngrp;
+  const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
+  p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
+  p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
+  const dim3 grid(static_cast<unsigned>(pl.nsplit_max), static_cast<unsigned>(c.n_kv_heads),
+                  static_cast<unsigned>(a.batch));
+  cudaError_t e;
+  if (a.head_dim == 128)
+    e = pl.nt == 1 ? launch_decode_d128_nt1(c.k_fmt, c.v_fmt, p, grid, pl.smem, st)
+                   : launch_decode_d128_nt2(c.k_fmt, c.v_fmt, p, grid, pl.smem, st);
+  else
+    e = launch_decode_d256_nt1(c.k_fmt, c.v_fmt, p, grid, pl.smem, st);
+  return cuda_status(e);
+}
+
+int run_combine(const memra_kv_cache *c, const int32_t *seq_lens, int32_t max_seq_len, int32_t max_pages,
+                int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, const void *workspace, void *out,
+                cudaStream_t st) {
+  size_t lse_off = 0;
+  workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len, &lse_off);
+  CombineParams p;
+  p.seq_lens = seq_lens;
+  p.o_part = static_cast<const float *>(workspace);
+  p.lse_part = reinterpret_cast<const float *>(static_cast<const uint8_t *>(workspace) + lse_off);
+  p.out = static_cast<__half *>(out);
+  p.status = c->status;
+  p.rows = batch * q_len * n_heads;
+  p.q_len = q_len;
+  p.n_heads = n_heads;
+  p.max_seq_len = max_seq_len;
+  p.max_pages = max_pages;
+  p.nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
+  return cuda_status(launch_combine(head_dim, p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t memra_kv_segment_bytes(int32_t fmt, int32_t is_v, int32_t head_dim) {
+  if (head_dim != 128 && head_dim != 256) return 0;
+  if (is_v == 0) return k_format_ok(fmt) ? static_cast<size_t>(k_seg_bytes(fmt, head_dim)) : 0;
+  if (is_v == 1) return v_format_ok(fmt) ? static_cast<size_t>(v_seg_bytes(fmt, head_dim)) : 0;
+  return 0;
+}
+
+size_t memra_kv_pool_bytes(int32_t fmt, int32_t is_v, int32_t num_pages, int32_t page_size, int32_t n_kv_heads,
+                           int32_t head_dim) {
+  if (page_size != MEMRA_PAGE_SIZE || num_pages < 1 || n_kv_heads < 1) return 0;
+  return memra_kv_segment_bytes(fmt, is_v, head_dim) * static_cast<size_t>(num_pages) * n_kv_heads;
+}
+
+int memra_kv_append(const memra_kv_cache *cache, const void *k, const void *v, const int32_t *slot_mapping,
+                    int32_t n_tok, void *stream) {
+  int st = check_cache(cache);
+  if (st) return st;
+  if (n_tok < 0) return MEMRA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MEMRA_OK;
+  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
+    return MEMRA_ERR_INVALID_ARG;
+  return cuda_status(launch_kv_append(*cache, k, v, slot_mapping, n_tok, static_cast<cudaStream_t>(stream)));
+}
+
+size_t memra_decode_attn_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim,
+                                         int32_t max_seq_len) {
+  if (batch < 0 || q_len < 1 || n_heads < 1 || (head_dim != 128 && head_dim != 256) || max_seq_len < 0) return 0;
+  return workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len, nullptr);
+}
+
+int memra_decode_attn_partials(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                               int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                               int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
+                               void *workspace, size_t workspace_bytes, void *out, void *stream) {
+  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
+  int st = check_decode(a);
+  if (st || batch == 0) return st;
+  return run_partials(a, static_cast<cudaStream_t>(stream));
+}
+
+int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t max_pages_per_seq, int32_t batch, int32_t q_len, int32_t n_heads,
+                              int32_t head_dim, const void *workspace, size_t workspace_bytes, void *out,
+                              void *stream) {
+  int st = check_cache(cache);
+  if (st) return st;
+  if (batch < 0 || q_len < 1 || n_heads < 1 || max_seq_len < 0 || head_dim != cache->head_dim ||
+      max_pages_per_seq < 0)
+    return MEMRA_ERR_INVALID_ARG;
+  if (batch == 0) return MEMRA_OK;
+  if (!seq_lens || !out || !aligned16(out)) return MEMRA_ERR_INVALID_ARG;
+  const size_t need = workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len, nullptr);
+  if (workspace_bytes < need) return MEMRA_ERR_WORKSPACE;
+  if (need > 0 && (!workspace || !aligned16(workspace))) return MEMRA_ERR_INVALID_ARG;
+  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
+                     out, static_cast<cudaStream_t>(stream));
+}
+
+int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                      int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                      int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
+                      void *workspace, size_t workspace_bytes, void *out, void *stream) {
+  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
+  int st = check_decode(a);
+  if (st || batch == 0) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_partials(a, s);
+  if (st) return st;
+  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
+                     out, s);
+}
+
+int memra_read_status(const memra_kv_cache *cache, int32_t *flags, void *stream) {
+  if (!cache || !flags) return MEMRA_ERR_INVALID_ARG;
+  *flags = 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MEMRA_ERR_CUDA;
+  if (!cache->status) return MEMRA_OK;
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, cache->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MEMRA_ERR_CUDA;
+  if (cudaMemsetAsync(cache->status, 0, sizeof(int32_t), s) != cudaSuccess) return MEMRA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MEMRA_ERR_CUDA;
+  *flags = host;
+  return host ? MEMRA_ERR_DEVICE : MEMRA_OK;
+}
+
+const char *memra_status_string(int status) {
+  switch (status) {
+    case MEMRA_OK: return "ok";
+    case MEMRA_ERR_INVALID_ARG: return "invalid argument";
+    case MEMRA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MEMRA_ERR_WORKSPACE: return "workspace too small";
+    case MEMRA_ERR_CUDA: return "CUDA error";
+    case MEMRA_ERR_DEVICE: return "the device flagged an error (see the status bits)";
+    default: return "unknown status";
+  }
+}
+
+int32_t memra_num_splits(int32_t seq_len) {
+  return seq_len <= 0 ? 0 : static_cast<int32_t>(ceil_div(seq_len, kSplitTokens));
+}
+
+}  // extern "C"

@@ -1,0 +1,564 @@
+// K2: split-K flash-decoding over the block-quantized paged KV cache.
+//
+// What it computes: for one (sequence, KV head, split of 1024 tokens), the
+// partial softmax(q K^T * scale) V over the split's keys for all the query
+// rows that read this KV head (the head's GQA group times q_len, causal among
+// the q_len new tokens), as (o = O / l, lse = m + log2 l).  The KV formats are
+// the memra-bench card's knobs (section "drafts/kf4/ - archived experiment");
+// plain decode and MTP verify are the memra README's "Speculative decoding"
+// item; the 262,144-token contexts its "Long context and larger models" item.
+//
+// How (one CTA = 4 consumer warps + 1 producer warp):
+//  * The producer warp reads the split's page ids and streams each page's K
+//    and V segments (one contiguous bulk copy each, 16-byte aligned, evict-
+//    first in L2) into a ring of shared-memory stages guarded by mbarriers.
+//  * Consumer warp w takes every R-th page (R = 4 / row groups).  Per page:
+//    S^T[16 tokens x 8 rows] = K^ Q^T on the tensor cores (m16n8k16, fp16 in,
+//    fp32 out) with the K codes converted to fp16 in registers; the q8_0 block
+//    scale multiplies each 32-element block's partial sum, so K^ is exact.
+//    Online softmax in the fp32 accumulators (row max over the 8 token lanes
+//    by xor-shuffles), P transposed in registers (movmatrix) into the B
+//    operand, then O^T[D x rows] += V^T P^T with the V codes converted in
+//    registers and the per-token block scale folded into P; q5_1's +m term is
+//    one extra MMA (blocks x tokens) * P^T.
+//  * At the end the consumer warps merge their (m, l, O) through shared
+//    memory; a split that covers the whole sequence writes fp16 output,
+//    otherwise an fp32 partial for the combine kernel.
+// Every wait is bounded (MEMRA_DEVERR_TIMEOUT); bad page ids are skipped
+// (MEMRA_DEVERR_BAD_PAGE); tokens past seq_len never reach the result, even if
+// their bytes are garbage.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "memra_device.cuh"
+
+namespace memra {
+
+struct DecodeParams {
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const __half *q;
+  const int32_t *page_table;
+  const int32_t *seq_lens;
+  __half *out;
+  float *o_part;      // [rows][nsplit_max][D]
+  float *lse_part;    // [rows][nsplit_max]
+  int32_t *status;
+  int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group, qg;
+  int nsplit_max, num_stages, ngrp;
+  float scale_log2, v_scale;
+};
+
+struct CombineParams {
+  const int32_t *seq_lens;
+  const float *o_part;
+  const float *lse_part;
+  __half *out;
+  int32_t *status;
+  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max;
+};
+
+cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
+cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
+                             cudaStream_t stream);
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+template <int D, int NT>
+struct MergeLayout {
+  static constexpr int kRowsW = 8 * NT;
+  static constexpr int kNb = D / 32;
+  static constexpr int kO = kConsumerWarps * kRowsW * D;          // floats
+  static constexpr int kM = kConsumerWarps * kRowsW;
+  static constexpr int kTerm = kConsumerWarps * kRowsW * kNb;
+  static constexpr int kBytes = (kO + 2 * kM + kTerm) * 4;
+};
+
+// Context length after the same clamping the combine kernel applies.
+__device__ __forceinline__ int clamp_seq_len(int T, int q_len, int max_seq_len, int max_pages, int32_t *status,
+                                             bool report) {
+  int Tc = min(T, min(max_seq_len, max_pages * kPage));
+  Tc = max(Tc, 0);
+  if (report && (Tc != T || T < q_len)) flag_error(status, MEMRA_DEVERR_BAD_SEQ_LEN);
+  return Tc;
+}
+
+// q8_0 code pair -> fp16 pair, exact: bias to unsigned, splice under the
+// exponent of 1024, subtract 1152.
+__device__ __forceinline__ uint32_t i8pair_lo(uint32_t biased) {
+  return hsub2_u32(__byte_perm(biased, 0x64646464u, 0x4140), 0x64806480u);
+}
+__device__ __forceinline__ uint32_t i8pair_hi(uint32_t biased) {
+  return hsub2_u32(__byte_perm(biased, 0x64646464u, 0x4342), 0x64806480u);
+}
+
+template <int KF>
+__device__ __forceinline__ void k_pairs(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  if constexpr (KF == MEMRA_KV_Q8_0) {
+    const uint32_t bw = w ^ 0x80808080u;
+    lo = i8pair_lo(bw);
+    hi = i8pair_hi(bw);
+  } else {
+    lo = e4m3x2_to_half2(w & 0xFFFFu);
+    hi = e4m3x2_to_half2(w >> 16);
+  }
+}
+
+template <int SH>
+__device__ __forceinline__ uint32_t shift_const(uint32_t x) {
+  if constexpr (SH >= 0) return x >> SH;
+  else return x << (-SH);
+}
+
+template <int D, int KF, int VF, int NT>
+__global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decode_split_kernel(const DecodeParams p) {
+  constexpr int NB = D / 32;
+  constexpr int KSEG = k_seg_bytes(KF, D);
+  constexpr int VSEG = v_seg_bytes(VF, D);
+  constexpr int STAGE = KSEG + VSEG;
+  using ML = MergeLayout<D, NT>;
+  constexpr int ROWS_W = ML::kRowsW;
+  constexpr bool kQ5 = VF == MEMRA_KV_Q5_1;
+  constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
+  constexpr bool kVq = kQ5 || kQ4;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status,
+                              split == 0 && kvh == 0 && threadIdx.x == 0);
+  const int tok0 = split * kSplitTokens;
+  if (tok0 >= T) return;
+  const int npages = (min(T, tok0 + kSplitTokens) - tok0 + kPage - 1) / kPage;
+  const int nsplit_b = (T + kSplitTokens - 1) / kSplitTokens;
+
+  const int NS = p.num_stages;
+  const int region = max(NS * STAGE, ML::kBytes);
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t full0 = ring + region;
+  const uint32_t empty0 = full0 + 8 * NS;
+  int *page_ok = reinterpret_cast<int *>(smem + region + 16 * NS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngrp = p.ngrp;
+  const int R = kConsumerWarps / ngrp;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, ngrp);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer --
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages + tok0 / kPage;
+    const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG;
+    const size_t vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
+    const uint8_t *kbase = p.k_pool + static_cast<size_t>(kvh) * KSEG;
+    const uint8_t *vbase = p.v_pool + static_cast<size_t>(kvh) * VSEG;
+    int alive = 1;
+    int issued = 0;
+    for (int base = 0; base < npages && alive; base += 32) {
+      const int idx = base + lane;
+      int pid = idx < npages ? pt[idx] : 0;
+      const int ok = (pid >= 0 && pid < p.num_pages) ? 1 : 0;
+      if (idx < npages && !ok) flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+      const int cnt = min(32, npages - base);
+      for (int j = 0; j < cnt; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, pid, j);
+        const int okj = __shfl_sync(0xffffffffu, ok, j);
+        if (lane == 0) {
+          const int i = base + j, s = i % NS;
+          if (i >= NS) alive = mbar_wait_bounded(empty0 + 8 * s, ((i / NS) - 1) & 1, p.status) ? 1 : 0;
+          if (alive) {
+            page_ok[s] = okj;
+            if (okj) {
+              mbar_arrive_expect_tx(full0 + 8 * s, STAGE);
+              bulk_copy_g2s(ring + s * STAGE, kbase + static_cast<size_t>(pj) * kstride, KSEG, full0 + 8 * s, pol);
+              bulk_copy_g2s(ring + s * STAGE + KSEG, vbase + static_cast<size_t>(pj) * vstride, VSEG, full0 + 8 * s,
+                            pol);
+            } else {
+              mbar_arrive(full0 + 8 * s);
+            }
+            ++issued;
+          }
+        }
+        alive = __shfl_sync(0xffffffffu, alive, 0);
+        if (!alive) break;
+      }
+    }
+    // Stay until every copy this warp issued has landed (bounded), so no bulk
+    // copy can outlive the CTA's shared memory even if a consumer gave up.
+    if (lane == 0) {
+      for (int i = max(0, issued - NS); i < issued; ++i) {
+        if (!mbar_wait_bounded(full0 + 8 * (i % NS), (i / NS) & 1, p.status)) break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers --
+  const int gr = warp % ngrp, r = warp / ngrp;
+  const int g = lane >> 2, c = lane & 3;
+  const int row_base = gr * ROWS_W;
+
+  // Q^T fragments (B operand of S^T = K^ Q^T): row 8n+g, dims 32bb+8c..+7.
+  uint4 qf[NT][NB];
+  int lastv[NT][2];     // last visible key of the thread's rows 8n+2c+u
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int nr = row_base + 8 * n + g;
+    if (nr < p.qg) {
+      const int qi = nr / p.group, head = kvh * p.group + nr % p.group;
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          p.q + ((static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head) * D + 8 * c);
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = src[4 * bb];
+    } else {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int row = row_base + 8 * n + 2 * c + u;
+      lastv[n][u] = row < p.qg ? T - p.q_len + row / p.group : 0x7fffffff;
+    }
+  }
+  const int min_last = T - p.q_len;    // last key every real row sees
+
+  float o[NT][2 * NB][4];
+  float mt[NT][4];
+  float mrow[NT][2], lrow[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+#pragma unroll
+    for (int i = 0; i < 2 * NB; ++i) o[n][i][0] = o[n][i][1] = o[n][i][2] = o[n][i][3] = 0.f;
+    mt[n][0] = mt[n][1] = mt[n][2] = mt[n][3] = 0.f;
+    mrow[n][0] = mrow[n][1] = -INFINITY;
+    lrow[n][0] = lrow[n][1] = 0.f;
+  }
+
+  for (int i = r; i < npages; i += R) {
+    const int s = i % NS;
+    if (!mbar_wait_bounded(full0 + 8 * s, (i / NS) & 1, p.status)) break;
+    if (page_ok[s]) {
+      const uint32_t ka = ring + s * STAGE;
+      const uint32_t va = ka + KSEG;
+      const int pos0 = tok0 + i * kPage;
+      const bool masked = pos0 + kPage - 1 > min_last;
+      const bool partial = pos0 + kPage > T;
+
+      // ---------------------------------------------------- S^T = K^ Q^T --
+      float sc[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      {
+        uint4 kc[NB];
+#pragma unroll
+        for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
+        // q8_0 block scales of tokens g and g+8, two fp16 per word
+        uint32_t dk0[NB / 2], dk1[NB / 2];
+        if constexpr (KF == MEMRA_KV_Q8_0) {
+          if constexpr (NB == 4) {
+            const uint2 a = lds64(ka + 16 * D + g * NB * 2), bq = lds64(ka + 16 * D + (g + 8) * NB * 2);
+            dk0[0] = a.x; dk0[1] = a.y; dk1[0] = bq.x; dk1[1] = bq.y;
+          } else {
+            const uint4 a = lds128(ka + 16 * D + g * NB * 2), bq = lds128(ka + 16 * D + (g + 8) * NB * 2);
+            dk0[0] = a.x; dk0[1] = a.y; dk0[2] = a.z; dk0[3] = a.w;
+            dk1[0] = bq.x; dk1[1] = bq.y; dk1[2] = bq.z; dk1[3] = bq.w;
+          }
+        }
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          const uint4 &c0 = kc[bb / 2];
+          const uint4 &c1 = kc[NB / 2 + bb / 2];
+          const uint32_t t0lo = (bb & 1) ? c0.z : c0.x, t0hi = (bb & 1) ? c0.w : c0.y;
+          const uint32_t t1lo = (bb & 1) ? c1.z : c1.x, t1hi = (bb & 1) ? c1.w : c1.y;
+          uint32_t a0[4], a1[4];
+          k_pairs<KF>(t0lo, a0[0], a0[2]);
+          k_pairs<KF>(t1lo, a0[1], a0[3]);
+          k_pairs<KF>(t0hi, a1[0], a1[2]);
+          k_pairs<KF>(t1hi, a1[1], a1[3]);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            if constexpr (KF == MEMRA_KV_Q8_0) {
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
+              mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
+              const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
+              const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk1[bb / 2] >> (16 * (bb & 1)))));
+              sc[n][0] = fmaf(d0, acc[0], sc[n][0]);
+              sc[n][1] = fmaf(d0, acc[1], sc[n][1]);
+              sc[n][2] = fmaf(d1, acc[2], sc[n][2]);
+              sc[n][3] = fmaf(d1, acc[3], sc[n][3]);
+            } else {
+              mma_16816(sc[n], a0, qf[n][bb].x, qf[n][bb].y);
+              mma_16816(sc[n], a1, qf[n][bb].z, qf[n][bb].w);
+            }
+          }
+        }
+      }
+
+      // ------------------------------------------------- online softmax --
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        float s4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s4[e] = sc[n][e] * p.scale_log2;
+        if (masked) {
+          const int t0 = pos0 + g, t1 = pos0 + g + 8;
+          s4[0] = t0 <= lastv[n][0] ? s4[0] : -INFINITY;
+          s4[1] = t0 <= lastv[n][1] ? s4[1] : -INFINITY;
+          s4[2] = t1 <= lastv[n][0] ? s4[2] : -INFINITY;
+          s4[3] = t1 <= lastv[n][1] ? s4[3] : -INFINITY;
+        }
+        float p4[4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float mx = fmaxf(s4[u], s4[2 + u]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(mrow[n][u], mx);
+          const float muse = mnew == -INFINITY ? 0.f : mnew;
+          const float alpha = fast_exp2(mrow[n][u] - muse);
+          p4[u] = fast_exp2(s4[u] - muse);
+          p4[2 + u] = fast_exp2(s4[2 + u] - muse);
+          lrow[n][u] = fmaf(lrow[n][u], alpha, p4[u] + p4[2 + u]);
+          mrow[n][u] = mnew;
+#pragma unroll
+          for (int i2 = 0; i2 < 2 * NB; ++i2) {
+            o[n][i2][u] *= alpha;
+            o[n][i2][2 + u] *= alpha;
+          }
+          if constexpr (kQ5) mt[n][u] *= alpha;
+        }
+        pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
+        pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
+      }
+
+      // ---------------------------------------------- O^T += V^ P^T ---------
+      // token-validity masks of the thread's B/A token pairs (partial pages only)
+      uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+      if (partial) {
+        const int t = pos0 + 2 * c;
+        m01 = (t < T ? 0x0000FFFFu : 0u) | (t + 1 < T ? 0xFFFF0000u : 0u);
+        m89 = (t + 8 < T ? 0x0000FFFFu : 0u) | (t + 9 < T ? 0xFFFF0000u : 0u);
+      }
+      if constexpr (kVq) {
+        constexpr int DOFF = kQ5 ? 10 * D : 8 * D;
+        uint2 dv[NB];
+#pragma unroll
+        for (int q2 = 0; q2 < NB / 2; ++q2) {
+          const uint4 x = lds128(va + DOFF + c * NB * 8 + q2 * 16);
+          dv[2 * q2] = make_uint2(x.x & m01, x.y & m89);
+          dv[2 * q2 + 1] = make_uint2(x.z & m01, x.w & m89);
+        }
+        uint32_t hw[NB / 2];
+        if constexpr (kQ5) {
+          if constexpr (NB == 4) {
+            const uint2 x = lds64(va + 8 * D + lane * (NB / 2) * 4);
+            hw[0] = x.x;
+            hw[1] = x.y;
+          } else {
+            const uint4 x = lds128(va + 8 * D + lane * (NB / 2) * 4);
+            hw[0] = x.x; hw[1] = x.y; hw[2] = x.z; hw[3] = x.w;
+          }
+        }
+#pragma unroll
+        for (int bp = 0; bp < NB / 2; ++bp) {
+          const uint4 nw = lds128(va + (bp * 32 + lane) * 16);
+#pragma unroll
+          for (int bh = 0; bh < 2; ++bh) {
+            const int bb = 2 * bp + bh;
+            uint32_t bs[NT][2];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              bs[n][0] = hmul2_u32(pb[n][0], dv[bb].x);
+              bs[n][1] = hmul2_u32(pb[n][1], dv[bb].y);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t w = bh == 0 ? (h == 0 ? nw.x : nw.y) : (h == 0 ? nw.z : nw.w);
+              uint32_t a[4];
+#pragma unroll
+              for (int ii = 0; ii < 4; ++ii) {
+                uint32_t t = ((w >> (4 * ii)) & 0x000F000Fu) | 0x64006400u;
+                if constexpr (kQ5) {
+                  // bit 4 of the pair's codes sits at 8p + 4(bb%2) + 2h + s (+16 for the second token)
+                  const int sh = 8 * (ii >> 1) + 4 * bh + 2 * h + (ii & 1) - 4;
+                  const uint32_t x = sh >= 0 ? (hw[bp] >> sh) : (hw[bp] << (-sh));
+                  t |= x & 0x00100010u;
+                  a[ii] = hsub2_u32(t, 0x64006400u);
+                } else {
+                  a[ii] = hsub2_u32(t, 0x64086408u);
+                }
+              }
+#pragma unroll
+              for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, bs[n][0], bs[n][1]);
+            }
+          }
+        }
+        if constexpr (kQ5) {
+          uint2 mv = make_uint2(0, 0);
+          if (g < NB) {
+            mv = lds64(va + 11 * D + (c * NB + g) * 8);
+            mv.x &= m01;
+            mv.y &= m89;
+          }
+          const uint32_t am[4] = {mv.x, 0u, mv.y, 0u};
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            float acc[4] = {mt[n][0], mt[n][1], mt[n][2], mt[n][3]};
+            mma_16816(acc, am, pb[n][0], pb[n][1]);
+            mt[n][0] = acc[0]; mt[n][1] = acc[1]; mt[n][2] = acc[2]; mt[n][3] = acc[3];
+          }
+        }
+      } else {  // fp8 V
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          const uint4 x = lds128(va + (bb * 32 + lane) * 16);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t w0 = h == 0 ? x.x : x.z, w1 = h == 0 ? x.y : x.w;
+            uint32_t a[4];
+            a[0] = e4m3x2_to_half2(w0 & 0xFFFFu) & m01;
+            a[1] = e4m3x2_to_half2(w0 >> 16) & m01;
+            a[2] = e4m3x2_to_half2(w1 & 0xFFFFu) & m89;
+            a[3] = e4m3x2_to_half2(w1 >> 16) & m89;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, pb[n][0], pb[n][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+
+  // ------------------------------------------------------ merge the warps --
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float l = lrow[n][u];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      lrow[n][u] = l;
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);   // every consumer is done with the ring
+  float *mo = reinterpret_cast<float *>(smem);
+  float *mm = mo + ML::kO;
+  float *ml = mm + ML::kM;
+  float *mterm = ml + ML::kM;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int lr0 = warp * ROWS_W + 8 * n + 2 * c;
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j0 = 32 * bb + 4 * g + 2 * h;
+        mo[lr0 * D + j0] = o[n][2 * bb + h][0];
+        mo[(lr0 + 1) * D + j0] = o[n][2 * bb + h][1];
+        mo[lr0 * D + j0 + 1] = o[n][2 * bb + h][2];
+        mo[(lr0 + 1) * D + j0 + 1] = o[n][2 * bb + h][3];
+      }
+    }
+    if (g == 0) {
+      mm[lr0] = mrow[n][0];
+      mm[lr0 + 1] = mrow[n][1];
+      ml[lr0] = lrow[n][0];
+      ml[lr0 + 1] = lrow[n][1];
+    }
+    if constexpr (kQ5) {
+      if (g < NB) {
+        mterm[lr0 * NB + g] = mt[n][0];
+        mterm[(lr0 + 1) * NB + g] = mt[n][1];
+      }
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);
+
+  const int tid = threadIdx.x;
+  const float vscale = VF == MEMRA_KV_FP8_E4M3 ? p.v_scale : 1.f;
+  for (int item = tid; item < p.qg * (D / 4); item += kConsumerWarps * 32) {
+    const int nrow = item / (D / 4);
+    const int j4 = (item % (D / 4)) * 4;
+    const int grp = nrow / ROWS_W, lr = nrow % ROWS_W;
+    float M = -INFINITY;
+    for (int rr = 0; rr < R; ++rr) M = fmaxf(M, mm[(rr * ngrp + grp) * ROWS_W + lr]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+      for (int rr = 0; rr < R; ++rr) {
+        const int wr = (rr * ngrp + grp) * ROWS_W + lr;
+        const float wgt = fast_exp2(mm[wr] - M);
+        L = fmaf(wgt, ml[wr], L);
+        const float4 x = *reinterpret_cast<const float4 *>(mo + wr * D + j4);
+        const float add = kQ5 ? mterm[wr * NB + j4 / 32] : 0.f;
+        acc.x = fmaf(wgt, x.x + add, acc.x);
+        acc.y = fmaf(wgt, x.y + add, acc.y);
+        acc.z = fmaf(wgt, x.z + add, acc.z);
+        acc.w = fmaf(wgt, x.w + add, acc.w);
+      }
+    }
+    const float inv = L > 0.f ? vscale / L : 0.f;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    const int qi = nrow / p.group, head = kvh * p.group + nrow % p.group;
+    const size_t rowid = (static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head;
+    if (nsplit_b == 1) {
+      uint2 h;
+      h.x = pack_half2(acc.x, acc.y);
+      h.y = pack_half2(acc.z, acc.w);
+      *reinterpret_cast<uint2 *>(p.out + rowid * D + j4) = h;
+    } else {
+      const size_t pidx = rowid * p.nsplit_max + split;
+      *reinterpret_cast<float4 *>(p.o_part + pidx * D + j4) = acc;
+      if (j4 == 0) p.lse_part[pidx] = L > 0.f ? M + __log2f(L) : -INFINITY;
+    }
+  }
+}
+
+// One dispatcher per translation unit (head_dim, rows per warp).
+cudaError_t launch_decode_d128_nt1(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_decode_d128_nt2(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_decode_d256_nt1(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
+
+template <int D, int KF, int VF, int NT>
+cudaError_t launch_one(const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
+  static bool configured = false;   // per instantiation; attribute is per device function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, KF, VF, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  decode_split_kernel<D, KF, VF, NT><<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int NT>
+cudaError_t dispatch_formats(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
+  if (kf == MEMRA_KV_Q8_0) {
+    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q5_1, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q4_0, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_FP8_E4M3, NT>(p, grid, smem, st);
+  } else if (kf == MEMRA_KV_FP8_E4M3) {
+    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q5_1, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q4_0, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_FP8_E4M3, NT>(p, grid, smem, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace memra

@@ -1,0 +1,233 @@
+// K1: quantize-append of fp16 K/V rows into the block-quantized paged pools.
+//
+// Formats and rules: memra-bench card, "drafts/kf4/ - archived experiment"
+// (KV knobs K = q8_0 | fp8, V = q5_1 | q4_0 | fp8); the block rules and the
+// byte layout are the ones stated in include/memra.h.
+//
+// One group of D/8 lanes handles one (token, kv-head) row: each lane loads 8
+// consecutive fp16 elements with one 128-bit load (a 32-element block is four
+// lanes), block max/min come from two xor-shuffles, and the codes go straight
+// to the positions the decode kernel's fragments read.  The arithmetic of the
+// rules is done in float64 (x - m is not always exact in float32; the whole
+// append is a few hundred kilobytes per decode step).
+#include <cuda_runtime.h>
+
+#include "memra_device.cuh"
+
+namespace memra {
+
+struct AppendParams {
+  const __half *k;
+  const __half *v;
+  const int32_t *slots;
+  uint8_t *k_pool;
+  uint8_t *v_pool;
+  int32_t *status;
+  int n_tok, n_kv_heads, num_pages, k_fmt, v_fmt;
+  float k_scale, v_scale;
+};
+
+__device__ __forceinline__ float group4_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float group4_min(float x) {
+  x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fminf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+
+__device__ __forceinline__ void store_half(uint8_t *p, __half h) {
+  *reinterpret_cast<__half *>(p) = h;
+}
+
+// rne(num / d) with the stored fp16 d, in float64, clamped; 0 when d == 0.
+__device__ __forceinline__ int quant_code(double num, double d, int lo, int hi) {
+  if (d == 0.0) return 0;
+  int q = __double2int_rn(num / d);
+  return min(max(q, lo), hi);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kNb = D / 32;
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = gtid / kLanesPerRow;            // (token, kv-head)
+  const int l = gtid % kLanesPerRow;              // lane within the row
+  const bool live = row < p.n_tok * p.n_kv_heads;
+  const int tok = live ? row / p.n_kv_heads : 0;
+  const int head = live ? row % p.n_kv_heads : 0;
+  int slot = live ? p.slots[tok] : -1;
+  if (slot >= p.num_pages * kPage) {
+    if (l == 0) flag_error(p.status, MEMRA_DEVERR_BAD_SLOT);
+    slot = -1;
+  }
+  const bool act = live && slot >= 0;
+  const int page = act ? slot / kPage : 0;
+  const int t = act ? slot % kPage : 0;
+  const int b = l / 4;                            // block
+  const int cc = l % 4;                           // 8-element chunk within the block
+
+  // Both K and V of the row; shuffles below run on every lane (inactive rows
+  // carry zeros), stores only on active rows.
+  float xk[8], xv[8];
+  {
+    uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+    if (act) {
+      const size_t off = (static_cast<size_t>(tok) * p.n_kv_heads + head) * D + 8 * l;
+      rk = *reinterpret_cast<const uint4 *>(p.k + off);
+      rv = *reinterpret_cast<const uint4 *>(p.v + off);
+    }
+    const __half2 *hk = reinterpret_cast<const __half2 *>(&rk);
+    const __half2 *hv = reinterpret_cast<const __half2 *>(&rv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 a = __half22float2(hk[i]);
+      float2 c = __half22float2(hv[i]);
+      xk[2 * i] = a.x; xk[2 * i + 1] = a.y;
+      xv[2 * i] = c.x; xv[2 * i + 1] = c.y;
+    }
+  }
+
+  // ------------------------------------------------------------------ K ---
+  {
+    uint8_t *seg = p.k_pool + (static_cast<size_t>(page) * p.n_kv_heads + head) * k_seg_bytes(p.k_fmt, D);
+    const int tg = t % 8, tp = t / 8;
+    const int chunk = (tp * (kNb / 2) + b / 2) * 32 + 4 * tg + cc;
+    uint8_t code[8];
+    if (p.k_fmt == MEMRA_KV_Q8_0) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xk[i]));
+      amax = group4_max(amax);
+      const __half dh = __double2half(static_cast<double>(amax) / 127.0);
+      const double d = static_cast<double>(__half2float(dh));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(static_cast<int8_t>(quant_code(xk[i], d, -127, 127)));
+      if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        code[i] = __nv_cvt_float_to_fp8(__fdiv_rn(xk[i], p.k_scale), __NV_SATFINITE, __NV_E4M3);
+    }
+    if (act) {
+      uint2 w;
+      w.x = code[0] | (code[1] << 8) | (code[2] << 16) | (static_cast<uint32_t>(code[3]) << 24);
+      w.y = code[4] | (code[5] << 8) | (code[6] << 16) | (static_cast<uint32_t>(code[7]) << 24);
+      *reinterpret_cast<uint2 *>(seg + chunk * 16 + (b % 2) * 8) = w;
+    }
+  }
+
+  // ------------------------------------------------------------------ V ---
+  {
+    uint8_t *seg = p.v_pool + (static_cast<size_t>(page) * p.n_kv_heads + head) * v_seg_bytes(p.v_fmt, D);
+    const int c = (t % 8) / 2, f = t % 2, pp = t / 8, k = 2 * f + pp;
+    // element i of this lane: r = 8*cc + i -> vg = 2*cc + i/4, h = (i%4)/2, s = i%2
+    if (p.v_fmt == MEMRA_KV_FP8_E4M3) {
+      if (act) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int vg = 2 * cc + i / 4, h = (i % 4) / 2, s = i % 2;
+          const uint8_t byte = __nv_cvt_float_to_fp8(__fdiv_rn(xv[i], p.v_scale), __NV_SATFINITE, __NV_E4M3);
+          seg[(b * 32 + 4 * vg + c) * 16 + 8 * h + 2 * (2 * pp + s) + f] = byte;
+        }
+      }
+    } else {
+      int q[8];
+      __half dh, mh = __float2half(0.f);
+      if (p.v_fmt == MEMRA_KV_Q5_1) {
+        float mn = xv[0], mx = xv[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) { mn = fminf(mn, xv[i]); mx = fmaxf(mx, xv[i]); }
+        mn = group4_min(mn);
+        mx = group4_max(mx);
+        dh = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / 31.0);
+        mh = __float2half_rn(mn);                      // exact: mn is an fp16 value
+        const double d = static_cast<double>(__half2float(dh));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = quant_code(static_cast<double>(xv[i]) - static_cast<double>(mn), d, 0, 31);
+      } else {  // q4_0, nibble = q + 8
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xv[i]));
+        amax = group4_max(amax);
+        dh = __double2half(static_cast<double>(amax) / 7.0);
+        const double d = static_cast<double>(__half2float(dh));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], d, -8, 7) + 8;
+      }
+      // low nibbles: one byte per (vg, h) holding s = 0 (low) and s = 1 (high)
+      if (act) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int vg = 2 * cc + u;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i0 = 4 * u + 2 * h;
+            const uint8_t byte = static_cast<uint8_t>((q[i0] & 15) | ((q[i0 + 1] & 15) << 4));
+            seg[((b / 2) * 32 + 4 * vg + c) * 16 + (b % 2) * 8 + 4 * h + k] = byte;
+          }
+        }
+      }
+      if (p.v_fmt == MEMRA_KV_Q5_1) {
+        // bit 4 of each code: per vg a 4-bit group (bit 2h+s); blocks 2bp and
+        // 2bp+1 share a byte, so the even block's lane gathers its partner's.
+        uint32_t hn[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          hn[u] = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hn[u] |= static_cast<uint32_t>((q[4 * u + e] >> 4) & 1) << e;
+        }
+        const uint32_t mine = hn[0] | (hn[1] << 4);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 4);   // lane of block b^1
+        if (act && (b % 2) == 0) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int vg = 2 * cc + u;
+            const uint32_t lo = (mine >> (4 * u)) & 15u, hi = (other >> (4 * u)) & 15u;
+            seg[8 * D + ((4 * vg + c) * (kNb / 2) + b / 2) * 4 + k] = static_cast<uint8_t>(lo | (hi << 4));
+          }
+        }
+      }
+      if (act && cc == 0) {
+        const int poff = ((c * kNb + b) * 4 + 2 * pp + f) * 2;
+        if (p.v_fmt == MEMRA_KV_Q5_1) {
+          store_half(seg + 10 * D + poff, dh);
+          store_half(seg + 11 * D + poff, mh);
+        } else {
+          store_half(seg + 8 * D + poff, dh);
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
+                             cudaStream_t stream) {
+  AppendParams p;
+  p.k = static_cast<const __half *>(k);
+  p.v = static_cast<const __half *>(v);
+  p.slots = slots;
+  p.k_pool = static_cast<uint8_t *>(c.k_pool);
+  p.v_pool = static_cast<uint8_t *>(c.v_pool);
+  p.status = c.status;
+  p.n_tok = n_tok;
+  p.n_kv_heads = c.n_kv_heads;
+  p.num_pages = c.num_pages;
+  p.k_fmt = c.k_fmt;
+  p.v_fmt = c.v_fmt;
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  const long long rows = static_cast<long long>(n_tok) * c.n_kv_heads;
+  const long long threads = rows * (c.head_dim / 8);
+  const int block = 256;
+  const unsigned grid = static_cast<unsigned>((threads + block - 1) / block);
+  if (c.head_dim == 128)
+    kv_append_kernel<128><<<grid, block, 0, stream>>>(p);
+  else
+    kv_append_kernel<256><<<grid, block, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace memra

@@ -1,0 +1,196 @@
+/*
+ * memra.h - C ABI of the GB300 (sm_103a) decode-attention library for a
+ * block-quantized, paged KV cache.
+ *
+ * What the library computes (sources are the memra project pages):
+ *   - The KV-cache formats are the knobs named on the "memra-bench" card,
+ *     section "drafts/kf4/ - archived experiment": K = q8_0 | fp8,
+ *     V = q5_1 | q4_0 | fp8, defaults q8_0 / q5_1.
+ *   - Pages are the request-sized, reusable KV allocation of the memra
+ *     README ("Request reuse and admission" item of the serving surface);
+ *     several page tables may point at the same page (shared prefix, the
+ *     README introduction's 4,860-token shared-prefix serving shape).
+ *   - Query lengths: 1 (plain decode) and K+1 (MTP speculative verify,
+ *     README "Speculative decoding" item); contexts up to the 262,144 tokens
+ *     of the README's "Long context and larger models" item.
+ *
+ * Per-block rules (32 consecutive elements of one fp16 row along head_dim;
+ * rne = round half to even of the exact real value, using the stored fp16 d):
+ *   q8_0  d = fp16(max|x|/127),  q = clamp(rne(x/d), -127, 127),   x^ = d*q
+ *   q5_1  m = min x, d = fp16((max-min)/31), q = clamp(rne((x-m)/d), 0, 31),
+ *                                                                  x^ = d*q + m
+ *   q4_0  d = fp16(max|x|/7),    q = clamp(rne(x/d), -8, 7),       x^ = d*q
+ *   fp8   OCP e4m3 ("fn"): byte = rne_satfinite(fp32(x) / s), x^ = s*e4m3(byte),
+ *         s a float32 per-tensor scale given in memra_kv_cache.
+ *   A stored d of 0 gives q = 0.  Inputs must be finite.
+ *
+ * Attention: query row i of sequence b sits at position seq_lens[b]-q_len+i
+ * and sees keys 0..seq_lens[b]-q_len+i (causal among the q_len new tokens);
+ * query head h reads KV head h / (n_heads / n_kv_heads).  The output is
+ * softmax(q K^T * sm_scale) V^ over the dequantized cache, accumulated in
+ * float32, written as fp16.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers; the caller owns all
+ *     memory.  The library never allocates, frees or synchronizes on the
+ *     compute entry points; work is enqueued on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream).
+ *   - Return value: a memra_status.  Argument errors are detected on the host
+ *     before anything is enqueued.  Errors that only the GPU can see (a page
+ *     id outside the pool, a slot outside the pool, a seq_len larger than
+ *     the page table or max_seq_len, a pipeline wait that timed out) never
+ *     fault: the kernel skips the offending page / row and ORs a
+ *     MEMRA_DEVERR_* bit into *cache->status; memra_read_status reports it.
+ *   - All pointers must be 16-byte aligned; tensors are dense row-major.
+ *
+ * Pool layout (part of the ABI).  Each pool is
+ *   [num_pages][n_kv_heads][segment]
+ * and one segment holds one page (16 tokens) of one KV head.  D = head_dim,
+ * nb = D/32.  For token t (0..15) of the page and element j (0..D-1) of its
+ * row, b = j/32, r = j%32:
+ *   K q8_0 / fp8 codes: kc = r/8, e = r%8, tg = t%8, tp = t/8, lane = 4*tg+kc,
+ *       byte ((tp*(nb/2) + b/2)*32 + lane)*16 + (b%2)*8 + e
+ *   K q8_0 d:  16*D + (t*nb + b)*2                       (fp16, little endian)
+ *   V: vg = r/4, h = (r%4)/2, s = r%2, c = (t%8)/2, f = t%2, p = t/8,
+ *      lane = 4*vg + c, k = 2*f + p
+ *   V q5_1 / q4_0 low nibble (q5_1: q & 15; q4_0: q + 8):
+ *       byte ((b/2)*32 + lane)*16 + (b%2)*8 + 4*h + k, bits 4*s .. 4*s+3
+ *   V q5_1 bit 4 of q: byte 8*D + (lane*(nb/2) + b/2)*4 + k, bit 4*(b%2)+2*h+s
+ *   V q5_1 d: 10*D + ((c*nb + b)*4 + 2*p + f)*2,  m: 11*D + same offset
+ *   V q4_0 d: 8*D + ((c*nb + b)*4 + 2*p + f)*2
+ *   V fp8:    byte (b*32 + lane)*16 + 8*h + 2*(2*p + s) + f
+ * Segment bytes: K q8_0 17*D, K fp8 16*D, V q5_1 12*D, V q4_0 9*D,
+ * V fp8 16*D.  Every byte of a segment belongs to exactly one token, so
+ * appends to different slots never touch the same byte.  The order is the
+ * register-fragment order of the decode kernel's tensor-core tiles, so one
+ * bulk copy per segment lands the page in shared memory ready to read with
+ * conflict-free 16-byte loads.
+ */
+#ifndef MEMRA_H
+#define MEMRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+    MEMRA_OK = 0,
+    MEMRA_ERR_INVALID_ARG = 1,   /* a pointer, size or shape is not valid          */
+    MEMRA_ERR_UNSUPPORTED = 2,   /* valid, but outside what this build supports    */
+    MEMRA_ERR_WORKSPACE = 3,     /* workspace too small                            */
+    MEMRA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed           */
+    MEMRA_ERR_DEVICE = 5         /* memra_read_status: the device flagged an error */
+} memra_status;
+
+/* Bits the kernels OR into *memra_kv_cache.status. */
+#define MEMRA_DEVERR_BAD_PAGE    1   /* page id outside [0, num_pages): page skipped      */
+#define MEMRA_DEVERR_BAD_SLOT    2   /* append slot >= num_pages*16: row skipped          */
+#define MEMRA_DEVERR_BAD_SEQ_LEN 4   /* seq_len < q_len, > max_seq_len or > table: clamped */
+#define MEMRA_DEVERR_TIMEOUT     8   /* a pipeline wait gave up after ~1 s: result invalid */
+
+/* KV block formats (the memra-bench card's KV knobs). */
+typedef enum {
+    MEMRA_KV_Q8_0 = 0,       /* K only */
+    MEMRA_KV_Q5_1 = 1,       /* V only */
+    MEMRA_KV_Q4_0 = 2,       /* V only */
+    MEMRA_KV_FP8_E4M3 = 3    /* K or V */
+} memra_kv_format;
+
+/* Fixed page size (tokens) and the fixed token grid of the split-K plan. */
+#define MEMRA_PAGE_SIZE 16
+#define MEMRA_SPLIT_TOKENS 1024
+
+/* A paged KV cache.  Plain data; the caller owns the pools and status word. */
+typedef struct {
+    int32_t k_fmt;          /* memra_kv_format: MEMRA_KV_Q8_0 or MEMRA_KV_FP8_E4M3          */
+    int32_t v_fmt;          /* memra_kv_format: MEMRA_KV_Q5_1, MEMRA_KV_Q4_0 or _FP8_E4M3   */
+    int32_t page_size;      /* must be MEMRA_PAGE_SIZE                                      */
+    int32_t n_kv_heads;     /* >= 1                                                          */
+    int32_t head_dim;       /* 128 or 256                                                    */
+    int32_t num_pages;      /* pages in each pool, >= 1                                      */
+    void *k_pool;           /* device, memra_kv_pool_bytes(k_fmt, 0, ...) bytes              */
+    void *v_pool;           /* device, memra_kv_pool_bytes(v_fmt, 1, ...) bytes              */
+    float k_scale;          /* fp8 K: float32 per-tensor scale s (x^ = s*e4m3); else ignored */
+    float v_scale;          /* fp8 V: same for V                                             */
+    int32_t *status;        /* device int32 the kernels OR MEMRA_DEVERR_* bits into; may be NULL */
+} memra_kv_cache;
+
+/* Bytes of one segment (one page of one KV head) of a K (is_v = 0) or V
+ * (is_v = 1) pool; 0 if the format / side / head_dim combination is not
+ * supported.  Host only, no CUDA call. */
+size_t memra_kv_segment_bytes(int32_t fmt, int32_t is_v, int32_t head_dim);
+
+/* Bytes of a whole pool: num_pages * n_kv_heads * segment; 0 if unsupported.
+ * Host only, no CUDA call. */
+size_t memra_kv_pool_bytes(int32_t fmt, int32_t is_v, int32_t num_pages, int32_t page_size,
+                           int32_t n_kv_heads, int32_t head_dim);
+
+/* Quantize-append (the write side of the paged cache; formats as above).
+ *   k, v          device fp16 [n_tok][n_kv_heads][head_dim]
+ *   slot_mapping  device int32 [n_tok]; slot = page*16 + offset.  A negative
+ *                 slot skips the row (padding); a slot >= num_pages*16 skips
+ *                 it and sets MEMRA_DEVERR_BAD_SLOT.  Slots must be distinct
+ *                 within one call.
+ * n_tok == 0 is a no-op.  Results are bit-exact under the rules above. */
+int memra_kv_append(const memra_kv_cache *cache, const void *k, const void *v,
+                    const int32_t *slot_mapping, int32_t n_tok, void *stream);
+
+/* Workspace bytes memra_decode_attn needs for these sizes (the split-K
+ * partials: float32 [batch*q_len*n_heads][ceil(max_seq_len/1024)][head_dim]
+ * plus one float32 log-sum-exp per partial).  Host only. */
+size_t memra_decode_attn_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads,
+                                         int32_t head_dim, int32_t max_seq_len);
+
+/* Decode attention over the paged cache (split-K pass, then the combine).
+ *   q            device fp16 [batch][q_len][n_heads][head_dim]
+ *   page_table   device int32 [batch][max_pages_per_seq]; entries past
+ *                ceil(seq_lens[b]/16) are not read
+ *   seq_lens     device int32 [batch]; context of each sequence INCLUDING its
+ *                q_len new tokens (append them first with memra_kv_append)
+ *   max_seq_len  host upper bound of seq_lens (sizes the split grid)
+ *   n_kv_heads, head_dim must equal the cache's; n_heads % n_kv_heads == 0;
+ *   q_len*(n_heads/n_kv_heads) <= 64 (head_dim 128) or <= 32 (head_dim 256)
+ *   sm_scale     softmax scale (1/sqrt(head_dim) for standard attention)
+ *   workspace    device, >= memra_decode_attn_workspace_bytes(...) bytes
+ *   out          device fp16 [batch][q_len][n_heads][head_dim]
+ * batch == 0 is a no-op.  A sequence of length 0 yields zeros. */
+int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                      int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                      int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                      int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes,
+                      void *out, void *stream);
+
+/* The two passes of memra_decode_attn, separately (same arguments and
+ * meaning).  memra_decode_attn == partials followed by combine on one
+ * stream.  Sequences that fit one split are written to `out` by the
+ * partials pass directly; the combine pass merges the others. */
+int memra_decode_attn_partials(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                               int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                               int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                               int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes,
+                               void *out, void *stream);
+int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t max_pages_per_seq, int32_t batch, int32_t q_len, int32_t n_heads,
+                              int32_t head_dim, const void *workspace, size_t workspace_bytes, void *out,
+                              void *stream);
+
+/* Synchronizes `stream`, reads the device status word into *flags (0 if
+ * cache->status is NULL), clears it, and returns MEMRA_ERR_DEVICE if any bit
+ * was set, else MEMRA_OK (or MEMRA_ERR_CUDA if the stream reported an error). */
+int memra_read_status(const memra_kv_cache *cache, int32_t *flags, void *stream);
+
+/* Static English description of a memra_status value. */
+const char *memra_status_string(int status);
+
+/* Number of split-K partials a sequence of `seq_len` tokens produces. */
+int32_t memra_num_splits(int32_t seq_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEMRA_H */

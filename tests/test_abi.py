@@ -1,0 +1,112 @@
+"""The C ABI library loads, exports every declared symbol, and validates on the host (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "memra.h")
+
+
+@pytest.fixture(scope="module")
+def memra():
+    from decode_attention_block_memra_gb300 import _build
+    try:
+        _build.build()
+    except RuntimeError as e:          # no nvcc on this machine
+        pytest.skip(str(e))
+    import decode_attention_block_memra_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(memra_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(memra):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(memra.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_segment_and_pool_sizes(memra):
+    D = 128
+    assert memra.kv_segment_bytes("q8_0", False, D) == 17 * D
+    assert memra.kv_segment_bytes("fp8", False, D) == 16 * D
+    assert memra.kv_segment_bytes("q5_1", True, D) == 12 * D
+    assert memra.kv_segment_bytes("q4_0", True, 256) == 9 * 256
+    assert memra.kv_segment_bytes("fp8", True, 256) == 16 * 256
+    # K knobs are q8_0 | fp8 and V knobs q5_1 | q4_0 | fp8 only
+    assert memra.kv_segment_bytes("q5_1", False, D) == 0
+    assert memra.kv_segment_bytes("q8_0", True, D) == 0
+    assert memra.kv_segment_bytes("q8_0", False, 64) == 0
+    assert memra.kv_pool_bytes("q8_0", False, 16384, 4, 128) == 16384 * 4 * 2176
+    assert memra.kv_pool_bytes("q8_0", False, 10, 4, 128, page_size=32) == 0
+    from oracle import layout
+    for side, fmt in (("k", "q8_0"), ("k", "fp8"), ("v", "q5_1"), ("v", "q4_0"), ("v", "fp8")):
+        for D in (128, 256):
+            assert memra.kv_segment_bytes(fmt, side == "v", D) == layout.segment_bytes(side, fmt, D)
+
+
+def test_split_plan_and_workspace(memra):
+    assert memra.num_splits(0) == 0
+    assert memra.num_splits(1) == 1
+    assert memra.num_splits(1024) == 1
+    assert memra.num_splits(1025) == 2
+    assert memra.num_splits(262144) == 256
+    rows, ns, D = 1 * 1 * 32, 256, 128
+    o = rows * ns * D * 4
+    assert memra.decode_attn_workspace_bytes(1, 1, 32, 128, 262144) == ((o + 255) // 256) * 256 + rows * ns * 4
+    assert memra.decode_attn_workspace_bytes(4, 1, 8, 128, 0) == 0
+    assert memra.decode_attn_workspace_bytes(1, 0, 8, 128, 10) == 0
+
+
+def _cache(memra, **kw):
+    c = memra.KVCacheStruct(0, 1, 16, 2, 128, 4, 4096, 8192, 1.0, 1.0, 0)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _decode(memra, c, **kw):
+    a = dict(q=4096, pt=4096, maxp=4, sl=4096, maxlen=64, B=1, Q=1, Hq=8, Hkv=2, D=128, scale=0.1, ws=4096,
+             wsb=1 << 20, out=4096)
+    a.update(kw)
+    return memra.lib().memra_decode_attn(ctypes.byref(c), a["q"], a["pt"], a["maxp"], a["sl"], a["maxlen"], a["B"],
+                                         a["Q"], a["Hq"], a["Hkv"], a["D"], a["scale"], a["ws"], a["wsb"], a["out"],
+                                         None)
+
+
+def test_host_validation_without_gpu(memra):
+    """Every argument error is caught on the host before any CUDA call."""
+    L = memra.lib()
+    assert L.memra_kv_append(None, 16, 16, 16, 1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, k_fmt=1)), 16, 16, 16, 1, None) == 2    # q5_1 is not a K knob
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, v_fmt=0)), 16, 16, 16, 1, None) == 2    # q8_0 is not a V knob
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, page_size=32)), 16, 16, 16, 1, None) == 2
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, head_dim=64)), 16, 16, 16, 1, None) == 2
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, k_pool=4100)), 16, 16, 16, 1, None) == 1  # misaligned
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, k_fmt=3, k_scale=0.0)), 16, 16, 16, 1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra)), 16, 16, 16, -1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra)), 0, 16, 16, 1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra)), 16, 16, 16, 0, None) == 0               # no-op
+    c = _cache(memra)
+    assert _decode(memra, c, B=0) == 0                                  # empty batch: no-op
+    assert _decode(memra, c, Hq=7) == 1                                 # 7 query heads over 2 KV heads
+    assert _decode(memra, c, Hkv=4) == 1                                # disagrees with the cache
+    assert _decode(memra, c, D=256) == 1
+    assert _decode(memra, c, wsb=10) == 3                               # workspace too small
+    assert _decode(memra, c, q=4097) == 1
+    assert _decode(memra, c, scale=float("nan")) == 1
+    assert _decode(memra, c, Q=0) == 1
+    assert _decode(memra, c, Q=9, Hq=16) == 2                           # 72 rows per KV head
+    assert _decode(memra, _cache(memra, head_dim=256), D=256, Q=5, Hq=16) == 2   # 40 rows at D 256
+    assert L.memra_read_status(None, None, None) == 1
+    assert memra.status_string(3) == "workspace too small"
+    assert memra.status_string(99) == "unknown status"

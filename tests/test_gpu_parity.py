@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Quantized blocks must match the oracle bit for bit; attention outputs within
+max |gpu - oracle| <= 2e-3 (fp16 output of fp32-accumulated attention, see
+the tolerance derivation in the design doc).  The pools start as seeded random
+bytes, so slots that were never written hold garbage the kernels must ignore.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import attention, layout, quant
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_attention_block_memra_gb300 import _build
+    _build.build()
+    import decode_attention_block_memra_gb300 as memra
+    memra.lib()
+
+
+def run(w, fill_seed=1, want_pools=True):
+    from decode_attention_block_memra_gb300.runner import run_workload
+    return run_workload(w, fill_seed=fill_seed, want_pools=want_pools)
+
+
+def assert_pools_exact(w, res, cache=None):
+    kp, vp = attention.build_pools(w, cache=cache, fill=(res.initial_k_pool, res.initial_v_pool))
+    for name, want, got in (("K", kp, res.k_pool), ("V", vp, res.v_pool)):
+        if not np.array_equal(want, got):
+            bad = np.argwhere(want != got)
+            raise AssertionError(f"{name} pool differs at {len(bad)} bytes, first (page, head, byte) {bad[:5].tolist()}")
+
+
+def assert_rows_exact(w, res, rows, cache):
+    """Decode sampled rows from the GPU pools and compare their fields with the oracle's."""
+    for h in range(w.n_kv_heads):
+        for side, fmt, pool, scale in (("k", w.k_fmt, res.k_pool, w.k_scale), ("v", w.v_fmt, res.v_pool, w.v_scale)):
+            got = layout.read_rows(pool, side, fmt, w.slots[rows], h, w.head_dim, scale)
+            want = quant.select_rows(cache[side][h], rows)
+            for key in ("q", "d", "m"):
+                if key in want:
+                    a = np.asarray(got[key]).view(np.uint8)
+                    b = np.asarray(want[key]).view(np.uint8)
+                    assert np.array_equal(a, b), f"{side} {fmt} field {key} differs (head {h})"
+
+
+def assert_out_close(w, res, ref, tol=TOL):
+    mask = ~np.isnan(ref[..., 0])
+    got = res.out.astype(np.float64)[mask]
+    want = ref[mask]
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - want).max()
+    assert err <= tol, f"max |gpu - oracle| = {err:.3e} > {tol}"
+    return err
+
+
+# ------------------------------------------------------------ small cases ---
+
+def test_tiny_workload():
+    w = W.tiny()
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+FORMAT_PAIRS = [("q8_0", "q5_1"), ("q8_0", "q4_0"), ("q8_0", "fp8"), ("fp8", "q5_1"), ("fp8", "q4_0"),
+                ("fp8", "fp8")]
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kf,vf", FORMAT_PAIRS)
+def test_formats_ragged(kf, vf, D):
+    # 3 sequences, contexts spanning 1..3 splits with ragged tails, shuffled pages, GQA group 8
+    w = W.random_case(1000 + D + 7 * FORMAT_PAIRS.index((kf, vf)), batch=3, q_len=1, n_heads=16, n_kv_heads=2,
+                      head_dim=D, k_fmt=kf, v_fmt=vf, ctx=(5, 2600))
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("q_len,n_heads,n_kv_heads,D", [
+    (4, 32, 4, 128),     # MTP verify shape: 32 query rows per KV head (two row groups)
+    (2, 8, 2, 128),      # 8 rows
+    (3, 8, 2, 128),      # 12 rows: padded row group
+    (8, 64, 8, 128),     # 64 rows per KV head: four row groups
+    (1, 4, 4, 128),      # no grouping
+    (1, 12, 4, 256),     # group 3
+    (4, 16, 2, 256),     # 32 rows at D 256
+    (5, 4, 1, 256),      # 20 rows at D 256
+])
+def test_query_shapes(q_len, n_heads, n_kv_heads, D):
+    w = W.random_case(77 + q_len * 13 + n_heads + D, batch=2, q_len=q_len, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                      head_dim=D, ctx=(q_len, 2200))
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 1023, 1024, 1025, 2048, 2049])
+def test_context_edges(T):
+    w = W.make_workload(f"edge{T}", batch=1, q_len=1, n_heads=8, n_kv_heads=1, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=T, seq_lens=[T], permute_pages=True, extra_pages=2)
+    res = run(w)
+    assert res.flags == 0
+    ref = attention.reference(w)
+    assert_out_close(w, res, ref)
+    if T == 1:
+        # one visible key: the output is the dequantized V row (up to the fp16 output rounding)
+        cache = attention.quantize_cache(w)
+        v_hat = quant.dequantize_rows(cache["v"][0])[0]
+        for h in range(8):
+            assert np.abs(res.out[0, 0, h].astype(np.float64) - v_hat).max() <= np.abs(v_hat).max() * 2 ** -11 + 1e-7
+
+
+def test_causal_verify_rows_start_mid_page():
+    # q_len 6 with the new rows crossing a page and a split boundary
+    w = W.make_workload("verify_cross", batch=2, q_len=6, n_heads=8, n_kv_heads=2, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=3, seq_lens=[1027, 1030])
+    res = run(w)
+    assert res.flags == 0
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_shared_prefix_small():
+    w = W.make_workload("sp", batch=5, q_len=1, n_heads=16, n_kv_heads=2, head_dim=128, k_fmt="q8_0", v_fmt="q5_1",
+                        seed=8, seq_lens=[1100, 1300, 1031, 2100, 1024], shared_prefix=1024)
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_zero_query_and_constant_blocks():
+    # q = 0 -> uniform weights: the output is the mean of the visible V^ rows
+    w = W.random_case(5, batch=2, q_len=1, n_heads=8, n_kv_heads=2, ctx=(100, 1500))
+    w.q[:] = 0
+    w.v_rows[::3] = np.float16(0.75)          # flat blocks: q5_1 d = 0, x^ = m
+    w.k_rows[1::4] = np.float16(0.0)          # zero blocks: q8_0 d = 0
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    ref = attention.reference(w)
+    assert_out_close(w, res, ref)
+
+
+def test_empty_batch_and_empty_sequence():
+    import decode_attention_block_memra_gb300 as memra
+    w = W.random_case(9, batch=2, q_len=1, n_heads=8, n_kv_heads=2, ctx=(40, 300))
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w)
+    # batch 0: a no-op that touches nothing
+    memra.decode_attn(dw.cache, dw.q[:0], dw.page_table[:0], dw.seq_lens[:0], 0, dw.out[:0], dw.workspace)
+    # a sequence of length 0 gives zeros
+    dw.seq_lens[1] = 0
+    dw.out.fill_(7)
+    memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace, w.sm_scale)
+    flags = memra.read_status(dw.cache)
+    assert flags == memra.DEVERR_BAD_SEQ_LEN      # 0 < q_len is reported
+    assert torch.all(dw.out[1] == 0)
+
+
+def test_bad_page_and_slot_are_flagged_not_faulted():
+    import decode_attention_block_memra_gb300 as memra
+    w = W.random_case(11, batch=2, q_len=1, n_heads=8, n_kv_heads=2, ctx=(300, 900))
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w)
+    dw.page_table[0, 3] = w.num_pages + 5         # outside the pool
+    dw.page_table[1, 0] = -2
+    memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace, w.sm_scale)
+    assert memra.read_status(dw.cache) & memra.DEVERR_BAD_PAGE
+    assert torch.isfinite(dw.out.float()).all()
+    slots = dw.step_slots.clone()
+    slots[0] = w.num_pages * 16 + 1
+    slots[1] = -1                                  # padding: skipped silently
+    before = dw.cache.k_pool.clone()
+    memra.kv_append(dw.cache, dw.step_k, dw.step_v, slots)
+    assert memra.read_status(dw.cache) == memra.DEVERR_BAD_SLOT
+    assert torch.equal(before, dw.cache.k_pool)    # neither row was written
+
+
+def test_host_validation_errors():
+    import decode_attention_block_memra_gb300 as memra
+    w = W.random_case(12, batch=1, q_len=1, n_heads=8, n_kv_heads=2, ctx=(30, 60))
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w)
+    with pytest.raises(memra.MemraError) as e:
+        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace[:0])
+    assert e.value.status == 3
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(memra.MemraError):
+        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, 5000, dw.out, small_ws)
+    q3 = torch.zeros((1, 1, 6, 128), dtype=torch.float16, device="cuda")    # 6 heads over 2 KV heads? fine; 7 is not
+    q7 = torch.zeros((1, 1, 7, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(memra.MemraError) as e:
+        memra.decode_attn(dw.cache, q7, dw.page_table, dw.seq_lens, w.max_seq_len, torch.empty_like(q7), dw.workspace)
+    assert e.value.status == 1
+    del q3
+
+
+# ------------------------------------------------------ self-consistency ----
+
+def test_batch_invariance_and_determinism():
+    """A sequence's output bytes do not depend on the batch around it or on the run."""
+    w = W.random_case(31, batch=4, q_len=1, n_heads=32, n_kv_heads=4, ctx=(500, 3500))
+    full = run(w, want_pools=False)
+    again = run(w, want_pools=False)
+    assert np.array_equal(full.out.view(np.uint16), again.out.view(np.uint16))
+    for b in (0, 2):
+        solo = W.make_workload("solo", batch=1, q_len=1, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
+                               v_fmt="q5_1", seed=0, seq_lens=[int(w.seq_lens[b])])
+        rows = attention.sequence_rows(w, b)
+        solo.q[:] = w.q[b:b + 1]
+        solo.k_rows[:] = w.k_rows[rows]
+        solo.v_rows[:] = w.v_rows[rows]
+        r1 = run(solo, want_pools=False)
+        assert np.array_equal(r1.out[0].view(np.uint16), full.out[b].view(np.uint16))
+
+
+# ------------------------------------------------------ full-size workloads --
+
+def _sample_rows(w, n, seed):
+    rng = np.random.default_rng(seed)
+    B, Q, Hq, _ = w.q.shape
+    picks = {(int(rng.integers(B)), int(rng.integers(Q)), int(rng.integers(Hq))) for _ in range(n)}
+    picks.add((B - 1, Q - 1, Hq - 1))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["shared_prefix", "long_context", "mtp_verify"])
+def test_full_size_workloads(name):
+    w = W.WORKLOADS[name]()
+    cache = attention.quantize_cache(w)
+    res = run(w)
+    assert res.flags == 0
+    if name == "long_context":
+        rows = np.random.default_rng(0).choice(w.slots.size, 20000, replace=False)
+        rows = np.union1d(rows, w.step_rows)
+        assert_rows_exact(w, res, rows, cache)
+        assert_out_close(w, res, attention.reference(w, cache=cache))
+    else:
+        assert_pools_exact(w, res, cache=cache)
+        assert_out_close(w, res, attention.reference(w, cache=cache, rows=_sample_rows(w, 48, 1)))
+
+
+@pytest.fixture(scope="module")
+def sweep_base():
+    return W.format_sweep("c")
+
+
+@pytest.mark.parametrize("variant", ["a", "b", "c"])
+def test_format_sweep_full_size(sweep_base, variant):
+    kf, vf = W.SWEEP_FORMATS[variant]
+    w = sweep_base.with_formats(kf, vf)
+    res = run(w)
+    assert res.flags == 0
+    rows = np.random.default_rng(1).choice(w.slots.size, 4000, replace=False)
+    rows = np.union1d(rows, w.step_rows)
+    picks = _sample_rows(w, 24, 2)
+    seqs = sorted({b for b, _, _ in picks})
+    # oracle quantization of just the rows it needs
+    need = np.union1d(rows, np.concatenate([attention.sequence_rows(w, b) for b in seqs]))
+    cache = {"k": [], "v": []}
+    for h in range(w.n_kv_heads):
+        for side, fmt, src, sc in (("k", kf, w.k_rows, w.k_scale), ("v", vf, w.v_rows, w.v_scale)):
+            sub = quant.quantize_rows(src[need, h, :], fmt, sc)
+            full = {"fmt": fmt}
+            for key, val in sub.items():
+                if isinstance(val, np.ndarray):
+                    arr = np.zeros((w.slots.size,) + val.shape[1:], dtype=val.dtype)
+                    arr[need] = val
+                    full[key] = arr
+                elif key != "fmt":
+                    full[key] = val
+            cache[side].append(full)
+    assert_rows_exact(w, res, rows, cache)
+    assert_out_close(w, res, attention.reference(w, cache=cache, rows=picks))
