@@ -135,7 +135,7 @@ def test_causal_verify_rows_start_mid_page():
 
 def test_shared_prefix_small():
     w = W.make_workload("sp", batch=5, q_len=1, n_heads=16, n_kv_heads=2, head_dim=128, k_fmt="q8_0", v_fmt="q5_1",
-                        seed=8, seq_lens=[1100, 1300, 1031, 2100, 1024], shared_prefix=1024)
+                        seed=8, seq_lens=[1100, 1300, 1031, 2100, 1025], shared_prefix=1024)
     res = run(w)
     assert res.flags == 0
     assert_pools_exact(w, res)
