@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
     fence_barrier_init();
   }
   __syncthreads();
+  grid_dependency_wait();       // the append that precedes this launch has landed
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer --
@@ -527,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
       if (j4 == 0) p.lse_part[pidx] = L > 0.f ? M + __log2f(L) : -INFINITY;
     }
   }
+  allow_dependent_launch();
 }
 
 // One dispatcher per translation unit (head_dim, rows per warp).
@@ -543,8 +545,7 @@ cudaError_t launch_one(const DecodeParams &p, dim3 grid, size_t smem, cudaStream
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_split_kernel<D, KF, VF, NT><<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_split_kernel<D, KF, VF, NT>, grid, dim3(kThreads), smem, st, p);
 }
 
 template <int D, int NT>

@@ -7,9 +7,16 @@
 // One group of D/8 lanes handles one (token, kv-head) row: each lane loads 8
 // consecutive fp16 elements with one 128-bit load (a 32-element block is four
 // lanes), block max/min come from two xor-shuffles, and the codes go straight
-// to the positions the decode kernel's fragments read.  The arithmetic of the
-// rules is done in float64 (x - m is not always exact in float32; the whole
-// append is a few hundred kilobytes per decode step).
+// to the positions the decode kernel's fragments read.
+//
+// The rules round exact real quotients, so the arithmetic is exact in float32
+// (GB300's float64 rate is far too low for a hot path): x - m is carried as an
+// unevaluated pair hi + lo (Knuth's TwoSum), a candidate rounding comes from
+// one float32 division, and the candidate is then confirmed or moved by one
+// step by testing the sign of (hi - k*mid) + lo against the neighbouring
+// rounding midpoints mid, where k*mid and hi - k*mid are exact (few
+// significant bits; Sterbenz's lemma) and the final addition keeps the sign of
+// the exact sum.  Ties go to the even neighbour.
 #include <cuda_runtime.h>
 
 #include "memra_device.cuh"
@@ -40,17 +47,52 @@ __device__ __forceinline__ void store_half(uint8_t *p, __half h) {
   *reinterpret_cast<__half *>(p) = h;
 }
 
-// rne(num / d) with the stored fp16 d, in float64, clamped; 0 when d == 0.
-__device__ __forceinline__ int quant_code(double num, double d, int lo, int hi) {
-  if (d == 0.0) return 0;
-  int q = __double2int_rn(num / d);
-  return min(max(q, lo), hi);
+// a - b = hi + lo exactly (TwoSum of a and -b).
+__device__ __forceinline__ void two_diff(float a, float b, float &hi, float &lo) {
+  hi = __fsub_rn(a, b);
+  const float bb = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(-b, bb));
+}
+
+// fp16 round-to-nearest-even of (hi + lo) / k for hi + lo >= 0 and k in {7, 31, 127}.
+__device__ __forceinline__ __half fp16_quotient_rne(float hi, float lo, float k) {
+  unsigned short hb = __half_as_ushort(__float2half_rn(__fdiv_rn(hi, k)));
+  const float v = __half2float(__ushort_as_half(hb));
+  const float up_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb + 1))));
+  const float t_up = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, up_mid)), lo);     // sign of x/k - up_mid
+  if (t_up > 0.f || (t_up == 0.f && (hb & 1))) {
+    ++hb;
+  } else if (hb > 0) {
+    const float dn_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb - 1))));
+    const float t_dn = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, dn_mid)), lo);
+    if (t_dn < 0.f || (t_dn == 0.f && (hb & 1))) --hb;
+  }
+  return __ushort_as_half(hb);
+}
+
+// clamp(rne((hi + lo) / d), lo_q, hi_q) for the stored fp16 d (as float); 0 when d == 0.
+__device__ __forceinline__ int quant_code(float hi, float lo, float d, int lo_q, int hi_q) {
+  if (d == 0.f) return 0;
+  float q0 = rintf(__fdiv_rn(hi, d));
+  const float e = __fsub_rn(hi, __fmul_rn(q0, d));          // exact
+  const float hd = 0.5f * d;
+  const float up = __fadd_rn(__fsub_rn(e, hd), lo);          // sign of x/d - (q0 + 1/2)
+  const int odd = static_cast<int>(q0) & 1;
+  if (up > 0.f || (up == 0.f && odd)) {
+    q0 += 1.f;
+  } else {
+    const float dn = __fadd_rn(__fadd_rn(e, hd), lo);        // sign of x/d - (q0 - 1/2)
+    if (dn < 0.f || (dn == 0.f && odd)) q0 -= 1.f;
+  }
+  return min(max(static_cast<int>(q0), lo_q), hi_q);
 }
 
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kNb = D / 32;
+  grid_dependency_wait();        // k / v may come from the kernel before this one
+  allow_dependent_launch();      // the decode kernel may start its prologue
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int row = gtid / kLanesPerRow;            // (token, kv-head)
   const int l = gtid % kLanesPerRow;              // lane within the row
@@ -100,10 +142,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xk[i]));
       amax = group4_max(amax);
-      const __half dh = __double2half(static_cast<double>(amax) / 127.0);
-      const double d = static_cast<double>(__half2float(dh));
+      const __half dh = fp16_quotient_rne(amax, 0.f, 127.f);
+      const float d = __half2float(dh);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(static_cast<int8_t>(quant_code(xk[i], d, -127, 127)));
+      for (int i = 0; i < 8; ++i)
+        code[i] = static_cast<uint8_t>(static_cast<int8_t>(quant_code(xk[i], 0.f, d, -127, 127)));
       if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
     } else {
 #pragma unroll
@@ -141,20 +184,26 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
         for (int i = 1; i < 8; ++i) { mn = fminf(mn, xv[i]); mx = fmaxf(mx, xv[i]); }
         mn = group4_min(mn);
         mx = group4_max(mx);
-        dh = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / 31.0);
+        float rh, rl;
+        two_diff(mx, mn, rh, rl);
+        dh = fp16_quotient_rne(rh, rl, 31.f);
         mh = __float2half_rn(mn);                      // exact: mn is an fp16 value
-        const double d = static_cast<double>(__half2float(dh));
+        const float d = __half2float(dh);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = quant_code(static_cast<double>(xv[i]) - static_cast<double>(mn), d, 0, 31);
+        for (int i = 0; i < 8; ++i) {
+          float xh, xl;
+          two_diff(xv[i], mn, xh, xl);
+          q[i] = quant_code(xh, xl, d, 0, 31);
+        }
       } else {  // q4_0, nibble = q + 8
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xv[i]));
         amax = group4_max(amax);
-        dh = __double2half(static_cast<double>(amax) / 7.0);
-        const double d = static_cast<double>(__half2float(dh));
+        dh = fp16_quotient_rne(amax, 0.f, 7.f);
+        const float d = __half2float(dh);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], d, -8, 7) + 8;
+        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], 0.f, d, -8, 7) + 8;
       }
       // low nibbles: one byte per (vg, h) holding s = 0 (low) and s = 1 (high)
       if (act) {
@@ -223,11 +272,8 @@ cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void 
   const long long threads = rows * (c.head_dim / 8);
   const int block = 256;
   const unsigned grid = static_cast<unsigned>((threads + block - 1) / block);
-  if (c.head_dim == 128)
-    kv_append_kernel<128><<<grid, block, 0, stream>>>(p);
-  else
-    kv_append_kernel<256><<<grid, block, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (c.head_dim == 128) return launch_pdl(kv_append_kernel<128>, dim3(grid), dim3(block), 0, stream, p);
+  return launch_pdl(kv_append_kernel<256>, dim3(grid), dim3(block), 0, stream, p);
 }
 
 }  // namespace memra

@@ -286,3 +286,45 @@ def test_format_sweep_full_size(sweep_base, variant):
             cache[side].append(full)
     assert_rows_exact(w, res, rows, cache)
     assert_out_close(w, res, attention.reference(w, cache=cache, rows=picks))
+
+
+def _adversarial_rows(rng, n, D):
+    """fp16 rows whose 32-element blocks sit on rounding ties, subnormals and huge ranges."""
+    rows = rng.standard_normal((n, D))
+    for r in range(n):
+        for b in range(D // 32):
+            kind = (r * 7 + b) % 8
+            blk = rows[r, 32 * b:32 * b + 32]
+            if kind == 0:       # q8_0 ties at d = 1
+                blk[:] = np.concatenate([[127.0], np.arange(31) - 15.5])
+            elif kind == 1:     # q4_0 ties at d = 1
+                blk[:] = np.concatenate([[7.0], (np.arange(31) % 15) - 7.5])
+            elif kind == 2:     # q5_1 ties at d = 1, m = -1
+                blk[:] = np.concatenate([[-1.0, 30.0], np.arange(30) - 0.5])
+            elif kind == 3:     # huge range: x - m is not exact in float32
+                blk[:] = rng.standard_normal(32) * 1e-4
+                blk[0], blk[1] = 60000.0, -61000.0
+            elif kind == 4:     # fp16 subnormals only
+                blk[:] = rng.integers(-1023, 1024, 32) * 2.0 ** -24
+            elif kind == 5:     # flat subnormal block (d rounds far below max/7)
+                blk[:] = -2.0 ** -20
+            elif kind == 6:
+                blk[:] = rng.standard_normal(32) * 10.0 ** rng.uniform(-6, 3)
+    rows = rows.astype(np.float16)
+    rng.shuffle(rows)
+    return rows
+
+
+@pytest.mark.parametrize("kf,vf", [("q8_0", "q5_1"), ("q8_0", "q4_0")])
+def test_adversarial_blocks_bit_exact(kf, vf):
+    """Quantize-append is bit-exact on rounding ties, subnormal scales and extreme ranges."""
+    w = W.random_case(404, batch=2, q_len=1, n_heads=8, n_kv_heads=2, head_dim=128, k_fmt=kf, v_fmt=vf,
+                      ctx=(300, 700))
+    rng = np.random.default_rng(5)
+    n = w.k_rows.shape[0] * w.n_kv_heads
+    w.k_rows[:] = _adversarial_rows(rng, n, 128).reshape(w.k_rows.shape)
+    w.v_rows[:] = _adversarial_rows(rng, n, 128).reshape(w.v_rows.shape)
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert np.isfinite(res.out.astype(np.float32)).all()
