@@ -69,6 +69,9 @@ _SIGS = {
     "memra_decode_attn_combine": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p] +
                                   [ctypes.c_int32] * 6 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                           ctypes.c_void_p]),
+    "memra_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
+                                  [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
     "memra_read_status": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.POINTER(ctypes.c_int32),
                                          ctypes.c_void_p]),
     "memra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -201,6 +204,23 @@ def decode_attn_combine(cache: KVCache, seq_lens, max_seq_len: int, max_pages_pe
     _check(lib().memra_decode_attn_combine(cache.ref, _ptr(seq_lens), int(max_seq_len), int(max_pages_per_seq), batch,
                                            q_len, n_heads, cache.head_dim, _ptr(workspace), ws_bytes, _ptr(out),
                                            _stream(stream)), "memra_decode_attn_combine")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_attn_noalloc(cache: KVCache, q, page_table, seq_lens, max_seq_len: int, out, sm_scale=None,
+                        stream=None) -> None:
+    """memra_decode_attn_noalloc: decode attention without a workspace, for callers that cannot allocate.
+
+    The split-K partials go to a fixed library-owned device array of
+    NOALLOC_SCRATCH_BYTES; calls that may overlap on the GPU race on it.
+    """
+    B, Q, Hq, D = q.shape
+    _check(lib().memra_decode_attn_noalloc(cache.ref, _ptr(q), _ptr(page_table), int(page_table.shape[1]),
+                                           _ptr(seq_lens), int(max_seq_len), B, Q, Hq, cache.n_kv_heads, D,
+                                           float(sm_scale if sm_scale is not None else D ** -0.5), _ptr(out),
+                                           _stream(stream)), "memra_decode_attn_noalloc")
 
 
 def read_status(cache: KVCache, stream=None) -> int:

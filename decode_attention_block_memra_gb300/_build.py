@@ -17,7 +17,7 @@ BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libmemra.so")
 
 SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128_nt1.cu", "decode_d128_nt2.cu",
-           "decode_d256_nt1.cu"]
+           "decode_d256_nt1.cu", "noalloc.cu"]
 HEADERS = ["memra_device.cuh", "decode_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -178,6 +178,30 @@ int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_le
                               int32_t head_dim, const void *workspace, size_t workspace_bytes, void *out,
                               void *stream);
 
+/* Fixed size of the device array that memra_decode_attn_noalloc uses for the
+ * split-K partials (held on every device that calls it, until exit). */
+#define MEMRA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* memra_decode_attn for callers that cannot allocate device memory (code
+ * running inside a custom allocator or memory pool, plugins given only their
+ * input and output buffers, paths that forbid allocation after start-up).
+ * The memra pages have no counterpart of this call; it exists for such
+ * callers.  Same arguments and results as memra_decode_attn without the
+ * workspace: the partials go to a library-owned device array of
+ * MEMRA_NOALLOC_SCRATCH_BYTES, so the call allocates nothing.
+ *   - Returns MEMRA_ERR_WORKSPACE when memra_decode_attn_workspace_bytes(batch,
+ *     q_len, n_heads, head_dim, max_seq_len) exceeds MEMRA_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address (a CUDA
+ *     runtime query, no allocation); make that first call before any stream
+ *     capture.
+ *   - Every call shares the array and leaves its bytes behind; nothing in it
+ *     needs to start at zero.  Calls whose kernels may overlap on the GPU
+ *     (unordered streams) race on the array and must be serialized. */
+int memra_decode_attn_noalloc(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                              int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, float sm_scale, void *out, void *stream);
+
 /* Synchronizes `stream`, reads the device status word into *flags (0 if
  * cache->status is NULL), clears it, and returns MEMRA_ERR_DEVICE if any bit
  * was set, else MEMRA_OK (or MEMRA_ERR_CUDA if the stream reported an error). */
