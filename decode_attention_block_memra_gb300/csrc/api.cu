@@ -42,7 +42,7 @@ struct Plan {
 
 size_t merge_bytes(int D, int nt) {
   const size_t rows_w = 8 * nt, nb = D / 32;
-  const size_t w = kConsumerWarps;
+  const size_t w = kWarps;
   return (w * rows_w * D + 2 * w * rows_w + w * rows_w * nb) * 4;
 }
 
@@ -62,11 +62,15 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
     ngrp = static_cast<int>(ceil_div(qg, 8));
   }
   if (ngrp == 3) ngrp = 4;
-  if (ngrp > kConsumerWarps) return MEMRA_ERR_UNSUPPORTED;
+  if (ngrp > kWarps) return MEMRA_ERR_UNSUPPORTED;
+  // Pipeline depth: as many 16-token pages in flight as fit beside the CTAs
+  // that share an SM (4 CTAs of 4 warps at head_dim 128 with 8 rows per warp,
+  // else 2), in steps of 4 so that page i and page i + depth meet the same warp.
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
-  const size_t budget = 100 * 1024;
-  int ns = static_cast<int>(budget / stage);
-  if (ns > 16) ns = 16;
+  const int ctas_per_sm = (D == 128 && nt == 1) ? 4 : 2;
+  const size_t budget = (226 * 1024) / ctas_per_sm - 2048;
+  int ns = static_cast<int>(budget / stage) & ~3;
+  if (ns > 32) ns = 32;
   if (ns < 4) ns = 4;
   size_t region = stage * ns;
   const size_t mb = merge_bytes(D, nt);
@@ -76,7 +80,7 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   pl->qg = qg;
   pl->nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
   pl->num_stages = ns;
-  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(ns);
+  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(kSplitPages);
   return MEMRA_OK;
 }
 

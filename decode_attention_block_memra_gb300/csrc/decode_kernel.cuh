@@ -63,16 +63,16 @@ cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
 cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
                              cudaStream_t stream);
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
 
 template <int D, int NT>
 struct MergeLayout {
   static constexpr int kRowsW = 8 * NT;
   static constexpr int kNb = D / 32;
-  static constexpr int kO = kConsumerWarps * kRowsW * D;          // floats
-  static constexpr int kM = kConsumerWarps * kRowsW;
-  static constexpr int kTerm = kConsumerWarps * kRowsW * kNb;
+  static constexpr int kO = kWarps * kRowsW * D;          // floats
+  static constexpr int kM = kWarps * kRowsW;
+  static constexpr int kTerm = kWarps * kRowsW * kNb;
   static constexpr int kBytes = (kO + 2 * kM + kTerm) * 4;
 };
 
@@ -85,21 +85,12 @@ __device__ __forceinline__ int clamp_seq_len(int T, int q_len, int max_seq_len, 
   return Tc;
 }
 
-// q8_0 code pair -> fp16 pair, exact: bias to unsigned, splice under the
-// exponent of 1024, subtract 1152.
-__device__ __forceinline__ uint32_t i8pair_lo(uint32_t biased) {
-  return hsub2_u32(__byte_perm(biased, 0x64646464u, 0x4140), 0x64806480u);
-}
-__device__ __forceinline__ uint32_t i8pair_hi(uint32_t biased) {
-  return hsub2_u32(__byte_perm(biased, 0x64646464u, 0x4342), 0x64806480u);
-}
-
 template <int KF>
 __device__ __forceinline__ void k_pairs(uint32_t w, uint32_t &lo, uint32_t &hi) {
   if constexpr (KF == MEMRA_KV_Q8_0) {
-    const uint32_t bw = w ^ 0x80808080u;
-    lo = i8pair_lo(bw);
-    hi = i8pair_hi(bw);
+    // stored codes are q + 128: splice under the exponent of 1024 -> 1152 + q
+    lo = __byte_perm(w, 0x64646464u, 0x4140);
+    hi = __byte_perm(w, 0x64646464u, 0x4342);
   } else {
     lo = e4m3x2_to_half2(w & 0xFFFFu);
     hi = e4m3x2_to_half2(w >> 16);
@@ -113,7 +104,8 @@ __device__ __forceinline__ uint32_t shift_const(uint32_t x) {
 }
 
 template <int D, int KF, int VF, int NT>
-__global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128 ? 2 : 2)))
+    decode_split_kernel(const DecodeParams p) {
   constexpr int NB = D / 32;
   constexpr int KSEG = k_seg_bytes(KF, D);
   constexpr int VSEG = v_seg_bytes(VF, D);
@@ -123,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
   constexpr bool kQ5 = VF == MEMRA_KV_Q5_1;
   constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
   constexpr bool kVq = kQ5 || kQ4;
+  constexpr bool kK8 = KF == MEMRA_KV_Q8_0;
 
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -134,78 +127,61 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
   const int npages = (min(T, tok0 + kSplitTokens) - tok0 + kPage - 1) / kPage;
   const int nsplit_b = (T + kSplitTokens - 1) / kSplitTokens;
 
-  const int NS = p.num_stages;
+  const int NS = p.num_stages;                  // a multiple of 4, so page i and i + NS share a warp
   const int region = max(NS * STAGE, ML::kBytes);
   const uint32_t ring = smem_addr(smem);
   const uint32_t full0 = ring + region;
   const uint32_t empty0 = full0 + 8 * NS;
-  int *page_ok = reinterpret_cast<int *>(smem + region + 16 * NS);
+  int *pid_s = reinterpret_cast<int *>(smem + region + 16 * NS);   // page ids of this split, -1 = bad
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ngrp = p.ngrp;
-  const int R = kConsumerWarps / ngrp;
+  const int R = kWarps / ngrp;                  // page lanes
+  const int gr = warp % ngrp, r = warp / ngrp;  // row group, page lane
+  const bool issuer = gr == 0;                  // one warp per page lane issues its copies
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, ngrp);
     }
     fence_barrier_init();
   }
-  __syncthreads();
   grid_dependency_wait();       // the append that precedes this launch has landed
-
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer --
-    const uint64_t pol = l2_policy_evict_first();
+  {
     const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages + tok0 / kPage;
-    const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG;
-    const size_t vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
-    const uint8_t *kbase = p.k_pool + static_cast<size_t>(kvh) * KSEG;
-    const uint8_t *vbase = p.v_pool + static_cast<size_t>(kvh) * VSEG;
-    int alive = 1;
-    int issued = 0;
-    for (int base = 0; base < npages && alive; base += 32) {
-      const int idx = base + lane;
-      int pid = idx < npages ? pt[idx] : 0;
-      const int ok = (pid >= 0 && pid < p.num_pages) ? 1 : 0;
-      if (idx < npages && !ok) flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
-      const int cnt = min(32, npages - base);
-      for (int j = 0; j < cnt; ++j) {
-        const int pj = __shfl_sync(0xffffffffu, pid, j);
-        const int okj = __shfl_sync(0xffffffffu, ok, j);
-        if (lane == 0) {
-          const int i = base + j, s = i % NS;
-          if (i >= NS) alive = mbar_wait_bounded(empty0 + 8 * s, ((i / NS) - 1) & 1, p.status) ? 1 : 0;
-          if (alive) {
-            page_ok[s] = okj;
-            if (okj) {
-              mbar_arrive_expect_tx(full0 + 8 * s, STAGE);
-              bulk_copy_g2s(ring + s * STAGE, kbase + static_cast<size_t>(pj) * kstride, KSEG, full0 + 8 * s, pol);
-              bulk_copy_g2s(ring + s * STAGE + KSEG, vbase + static_cast<size_t>(pj) * vstride, VSEG, full0 + 8 * s,
-                            pol);
-            } else {
-              mbar_arrive(full0 + 8 * s);
-            }
-            ++issued;
-          }
-        }
-        alive = __shfl_sync(0xffffffffu, alive, 0);
-        if (!alive) break;
-      }
+    for (int i = tid; i < npages; i += kThreads) {
+      const int pid = pt[i];
+      const bool ok = pid >= 0 && pid < p.num_pages;
+      if (!ok) flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+      pid_s[i] = ok ? pid : -1;
     }
-    // Stay until every copy this warp issued has landed (bounded), so no bulk
-    // copy can outlive the CTA's shared memory even if a consumer gave up.
-    if (lane == 0) {
-      for (int i = max(0, issued - NS); i < issued; ++i) {
-        if (!mbar_wait_bounded(full0 + 8 * (i % NS), (i / NS) & 1, p.status)) break;
-      }
+  }
+  __syncthreads();
+
+  // Copies of page i into stage i % NS: one bulk copy each for the K and V
+  // segments, or a plain arrival for a skipped (bad) page.
+  const uint64_t pol = l2_policy_evict_first();
+  const uint8_t *kbase = p.k_pool + static_cast<size_t>(kvh) * KSEG;
+  const uint8_t *vbase = p.v_pool + static_cast<size_t>(kvh) * VSEG;
+  const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG;
+  const size_t vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
+  auto issue = [&](int i) {
+    const int s = i % NS;
+    const int pid = pid_s[i];
+    const uint32_t bar = full0 + 8 * s;
+    if (pid >= 0) {
+      mbar_arrive_expect_tx(bar, STAGE);
+      bulk_copy_g2s(ring + s * STAGE, kbase + static_cast<size_t>(pid) * kstride, KSEG, bar, pol);
+      bulk_copy_g2s(ring + s * STAGE + KSEG, vbase + static_cast<size_t>(pid) * vstride, VSEG, bar, pol);
+    } else {
+      mbar_arrive(bar);
     }
-    return;
+  };
+  if (issuer && lane == 0) {
+    for (int i = r; i < min(NS, npages); i += R) issue(i);
   }
 
-  // -------------------------------------------------------------- consumers --
-  const int gr = warp % ngrp, r = warp / ngrp;
   const int g = lane >> 2, c = lane & 3;
   const int row_base = gr * ROWS_W;
 
@@ -233,6 +209,27 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
   }
   const int min_last = T - p.q_len;    // last key every real row sees
 
+  // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q;
+  // the accumulator starts at -1152 * sum_j Q[row][j] over the block, which
+  // takes the bias back out inside the MMA.
+  float cq[NT][NB][2];
+  if constexpr (kK8) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&qf[n][bb]);
+        float2 a = __half22float2(h[0]), b2 = __half22float2(h[1]), c2 = __half22float2(h[2]),
+               d2 = __half22float2(h[3]);
+        float sum = ((a.x + a.y) + (b2.x + b2.y)) + ((c2.x + c2.y) + (d2.x + d2.y));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);          // row 8n+g, whole block
+#pragma unroll
+        for (int u = 0; u < 2; ++u) cq[n][bb][u] = -1152.f * __shfl_sync(0xffffffffu, sum, (2 * c + u) * 4);
+      }
+    }
+  }
+
   float o[NT][2 * NB][4];
   float mt[NT][4];
   float mrow[NT][2], lrow[NT][2];
@@ -245,10 +242,14 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
     lrow[n][0] = lrow[n][1] = 0.f;
   }
 
+  int s = r, par = 0;            // stage and phase parity of page i
+  int stop_at = -1;              // page whose wait gave up, if any
   for (int i = r; i < npages; i += R) {
-    const int s = i % NS;
-    if (!mbar_wait_bounded(full0 + 8 * s, (i / NS) & 1, p.status)) break;
-    if (page_ok[s]) {
+    if (!mbar_wait_bounded(full0 + 8 * s, par, p.status)) {
+      stop_at = i;
+      break;
+    }
+    if (pid_s[i] >= 0) {
       const uint32_t ka = ring + s * STAGE;
       const uint32_t va = ka + KSEG;
       const int pos0 = tok0 + i * kPage;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
         for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
         // q8_0 block scales of tokens g and g+8, two fp16 per word
         uint32_t dk0[NB / 2], dk1[NB / 2];
-        if constexpr (KF == MEMRA_KV_Q8_0) {
+        if constexpr (kK8) {
           if constexpr (NB == 4) {
             const uint2 a = lds64(ka + 16 * D + g * NB * 2), bq = lds64(ka + 16 * D + (g + 8) * NB * 2);
             dk0[0] = a.x; dk0[1] = a.y; dk1[0] = bq.x; dk1[1] = bq.y;
@@ -288,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
           k_pairs<KF>(t1hi, a1[1], a1[3]);
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
-            if constexpr (KF == MEMRA_KV_Q8_0) {
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (kK8) {
+              float acc[4] = {cq[n][bb][0], cq[n][bb][1], cq[n][bb][0], cq[n][bb][1]};
               mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
               mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
               const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
@@ -308,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
 
       // ------------------------------------------------- online softmax --
       uint32_t pb[NT][2];
+      float alpha[NT][2];
+      bool same = true;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         float s4[4];
@@ -328,21 +331,31 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const float mnew = fmaxf(mrow[n][u], mx);
+          same = same && (mnew == mrow[n][u]);
           const float muse = mnew == -INFINITY ? 0.f : mnew;
-          const float alpha = fast_exp2(mrow[n][u] - muse);
+          alpha[n][u] = fast_exp2(mrow[n][u] - muse);
           p4[u] = fast_exp2(s4[u] - muse);
           p4[2 + u] = fast_exp2(s4[2 + u] - muse);
-          lrow[n][u] = fmaf(lrow[n][u], alpha, p4[u] + p4[2 + u]);
+          lrow[n][u] = fmaf(lrow[n][u], alpha[n][u], p4[u] + p4[2 + u]);
           mrow[n][u] = mnew;
-#pragma unroll
-          for (int i2 = 0; i2 < 2 * NB; ++i2) {
-            o[n][i2][u] *= alpha;
-            o[n][i2][2 + u] *= alpha;
-          }
-          if constexpr (kQ5) mt[n][u] *= alpha;
         }
         pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
         pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
+      }
+      // the running maxima rarely move once a few pages are in: rescale only when one did
+      if (!__all_sync(0xffffffffu, same)) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int i2 = 0; i2 < 2 * NB; ++i2) {
+              o[n][i2][u] *= alpha[n][u];
+              o[n][i2][2 + u] *= alpha[n][u];
+            }
+            if constexpr (kQ5) mt[n][u] *= alpha[n][u];
+          }
+        }
       }
 
       // ---------------------------------------------- O^T += V^ P^T ---------
@@ -359,8 +372,15 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
 #pragma unroll
         for (int q2 = 0; q2 < NB / 2; ++q2) {
           const uint4 x = lds128(va + DOFF + c * NB * 8 + q2 * 16);
-          dv[2 * q2] = make_uint2(x.x & m01, x.y & m89);
-          dv[2 * q2 + 1] = make_uint2(x.z & m01, x.w & m89);
+          dv[2 * q2] = make_uint2(x.x, x.y);
+          dv[2 * q2 + 1] = make_uint2(x.z, x.w);
+        }
+        if (partial) {
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb) {
+            dv[bb].x &= m01;
+            dv[bb].y &= m89;
+          }
         }
         uint32_t hw[NB / 2];
         if constexpr (kQ5) {
@@ -411,16 +431,14 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
           uint2 mv = make_uint2(0, 0);
           if (g < NB) {
             mv = lds64(va + 11 * D + (c * NB + g) * 8);
-            mv.x &= m01;
-            mv.y &= m89;
+            if (partial) {
+              mv.x &= m01;
+              mv.y &= m89;
+            }
           }
           const uint32_t am[4] = {mv.x, 0u, mv.y, 0u};
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            float acc[4] = {mt[n][0], mt[n][1], mt[n][2], mt[n][3]};
-            mma_16816(acc, am, pb[n][0], pb[n][1]);
-            mt[n][0] = acc[0]; mt[n][1] = acc[1]; mt[n][2] = acc[2]; mt[n][3] = acc[3];
-          }
+          for (int n = 0; n < NT; ++n) mma_16816(mt[n], am, pb[n][0], pb[n][1]);
         }
       } else {  // fp8 V
 #pragma unroll
@@ -430,10 +448,13 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
           for (int h = 0; h < 2; ++h) {
             const uint32_t w0 = h == 0 ? x.x : x.z, w1 = h == 0 ? x.y : x.w;
             uint32_t a[4];
-            a[0] = e4m3x2_to_half2(w0 & 0xFFFFu) & m01;
-            a[1] = e4m3x2_to_half2(w0 >> 16) & m01;
-            a[2] = e4m3x2_to_half2(w1 & 0xFFFFu) & m89;
-            a[3] = e4m3x2_to_half2(w1 >> 16) & m89;
+            a[0] = e4m3x2_to_half2(w0 & 0xFFFFu);
+            a[1] = e4m3x2_to_half2(w0 >> 16);
+            a[2] = e4m3x2_to_half2(w1 & 0xFFFFu);
+            a[3] = e4m3x2_to_half2(w1 >> 16);
+            if (partial) {
+              a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+            }
 #pragma unroll
             for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, pb[n][0], pb[n][1]);
           }
@@ -441,7 +462,29 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    // Release the stage; the page lane's issuing warp refills it with page i + NS
+    // once every row group has released it.
+    if (lane == 0) {
+      mbar_arrive(empty0 + 8 * s);
+      if (issuer && i + NS < npages) {
+        if (mbar_wait_bounded(empty0 + 8 * s, par, p.status)) {
+          fence_proxy_async();
+          issue(i + NS);
+        }
+      }
+    }
+    s += R;
+    if (s >= NS) {
+      s -= NS;
+      par ^= 1;
+    }
+  }
+  // A wait that gave up: stay until this lane's copies in flight have landed
+  // (bounded), so no bulk copy outlives the CTA's shared memory.
+  if (stop_at >= 0 && issuer && lane == 0) {
+    for (int j = stop_at; j < min(stop_at + NS, npages); j += R) {
+      if (!mbar_wait_bounded(full0 + 8 * (j % NS), (j / NS) & 1, p.status)) break;
+    }
   }
 
   // ------------------------------------------------------ merge the warps --
@@ -456,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
       lrow[n][u] = l;
     }
   }
-  named_barrier_sync(1, kConsumerWarps * 32);   // every consumer is done with the ring
+  __syncthreads();                       // every warp is done with the ring
   float *mo = reinterpret_cast<float *>(smem);
   float *mm = mo + ML::kO;
   float *ml = mm + ML::kM;
@@ -488,11 +531,10 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 3 : 2)) decod
       }
     }
   }
-  named_barrier_sync(1, kConsumerWarps * 32);
+  __syncthreads();
 
-  const int tid = threadIdx.x;
   const float vscale = VF == MEMRA_KV_FP8_E4M3 ? p.v_scale : 1.f;
-  for (int item = tid; item < p.qg * (D / 4); item += kConsumerWarps * 32) {
+  for (int item = tid; item < p.qg * (D / 4); item += kThreads) {
     const int nrow = item / (D / 4);
     const int j4 = (item % (D / 4)) * 4;
     const int grp = nrow / ROWS_W, lr = nrow % ROWS_W;

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
       const float d = __half2float(dh);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        code[i] = static_cast<uint8_t>(static_cast<int8_t>(quant_code(xk[i], 0.f, d, -127, 127)));
+        code[i] = static_cast<uint8_t>(quant_code(xk[i], 0.f, d, -127, 127) + 128);   // stored biased
       if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
     } else {
 #pragma unroll

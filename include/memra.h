@@ -48,7 +48,8 @@
  * and one segment holds one page (16 tokens) of one KV head.  D = head_dim,
  * nb = D/32.  For token t (0..15) of the page and element j (0..D-1) of its
  * row, b = j/32, r = j%32:
- *   K q8_0 / fp8 codes: kc = r/8, e = r%8, tg = t%8, tp = t/8, lane = 4*tg+kc,
+ *   K q8_0 / fp8 codes (a q8_0 byte holds q + 128, an fp8 byte the e4m3 code):
+ *       kc = r/8, e = r%8, tg = t%8, tp = t/8, lane = 4*tg+kc,
  *       byte ((tp*(nb/2) + b/2)*32 + lane)*16 + (b%2)*8 + e
  *   K q8_0 d:  16*D + (t*nb + b)*2                       (fp16, little endian)
  *   V: vg = r/4, h = (r%4)/2, s = r%2, c = (t%8)/2, f = t%2, p = t/8,

@@ -12,7 +12,7 @@ Pool = [num_pages][n_kv_heads][segment]; a segment holds one page (16 tokens)
 of one KV head.  For token t (0..15) and element j (0..D-1) of its row, with
 nb = D/32, b = j // 32 and r = j % 32:
 
-K side (q8_0 codes and fp8 codes)
+K side (q8_0 codes, stored as the byte q + 128, and fp8 codes)
     kc = r // 8, e = r % 8, tg = t % 8, tp = t // 8, lane = 4 tg + kc
     code byte   ((tp (nb/2) + b//2) 32 + lane) 16 + (b%2) 8 + e
     q8_0 d      16 D + (t nb + b) 2                       (fp16, little endian)
@@ -131,7 +131,7 @@ def row_bytes(side: str, fields: dict, t: np.ndarray, D: int):
         if fmt not in ("q8_0", "fp8"):
             raise ValueError(f"K format {fmt} is not a K knob")
         offs.append(np.broadcast_to(k_code_offset(t, j, D), (N, D)))
-        vals.append(q.view(np.uint8) if q.dtype == np.int8 else q.astype(np.uint8))
+        vals.append((q.astype(np.int64) + 128).astype(np.uint8) if fmt == "q8_0" else q.astype(np.uint8))
         if fmt == "q8_0":
             bb = np.arange(nb, dtype=np.int64).reshape(1, nb)
             o = k_d_offset(t, bb, D)                                   # [N, nb]
@@ -208,7 +208,7 @@ def read_rows(pool: np.ndarray, side: str, fmt: str, slots: np.ndarray, head: in
     if side == "k":
         code = seg[page, k_code_offset(t, j, D)]
         if fmt == "q8_0":
-            return {"fmt": fmt, "q": code.view(np.int8), "d": f16_at(k_d_offset(t, bb, D))}
+            return {"fmt": fmt, "q": (code.astype(np.int64) - 128).astype(np.int8), "d": f16_at(k_d_offset(t, bb, D))}
         return {"fmt": fmt, "q": code, "scale": float(np.float32(scale))}
     if fmt in ("q5_1", "q4_0"):
         off, sh = v_nibble_offset(t, j, D)
