@@ -116,6 +116,13 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
   constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
   constexpr bool kVq = kQ5 || kQ4;
   constexpr bool kK8 = KF == MEMRA_KV_Q8_0;
+  // V codes enter the MMA with their fp16 offset (1024 + code, 1024 + 16 code);
+  // one extra MMA per block with an all-ones A sums the block's B operand, and
+  // the epilogue subtracts offset x sum (and divides slot g+8 by 16).  Used
+  // where the extra accumulators fit (8 query rows per warp).
+  constexpr bool kOnesMma = kVq && NT == 1;
+  constexpr float kLazy = 2.f;
+  const uint32_t kOnesA[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
 
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -166,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
   const uint8_t *vbase = p.v_pool + static_cast<size_t>(kvh) * VSEG;
   const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG;
   const size_t vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
-  auto issue = [&](int i) {
-    const int s = i % NS;
+  auto issue = [&](int i, int s) {      // page i into stage s
     const int pid = pid_s[i];
     const uint32_t bar = full0 + 8 * s;
     if (pid >= 0) {
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
     }
   };
   if (issuer && lane == 0) {
-    for (int i = r; i < min(NS, npages); i += R) issue(i);
+    for (int i = r; i < min(NS, npages); i += R) issue(i, i);
   }
 
   const int g = lane >> 2, c = lane & 3;
@@ -209,13 +215,17 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
   }
   const int min_last = T - p.q_len;    // last key every real row sees
 
-  // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q;
-  // the accumulator starts at -1152 * sum_j Q[row][j] over the block, which
-  // takes the bias back out inside the MMA.
-  float cq[NT][NB][2];
+  // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q,
+  // so block b's raw product is acc_b = sum_j q_j Q_j + 1152 sum_j Q_j.  The
+  // bias term of a token's score, sum_b d_b * 1152 * sumQ_b, is itself a small
+  // product [16 tokens x blocks] x [blocks x rows]: one more MMA per page with
+  // A = the page's block scales and B = -1152 sumQ_b split into fp16 hi + lo
+  // parts (k slots 0..nb-1 hi, nb..2nb-1 lo), exact to ~2^-22.
+  uint32_t corrb[NT][2];
   if constexpr (kK8) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
+      float csum[NB];
 #pragma unroll
       for (int bb = 0; bb < NB; ++bb) {
         const __half2 *h = reinterpret_cast<const __half2 *>(&qf[n][bb]);
@@ -224,20 +234,44 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
         float sum = ((a.x + a.y) + (b2.x + b2.y)) + ((c2.x + c2.y) + (d2.x + d2.y));
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);          // row 8n+g, whole block
-#pragma unroll
-        for (int u = 0; u < 2; ++u) cq[n][bb][u] = -1152.f * __shfl_sync(0xffffffffu, sum, (2 * c + u) * 4);
+        csum[bb] = -1152.f * sum;
       }
+      // B[k][row g]: thread (g, c) holds k = 2c, 2c+1 (b0b1) and 2c+8, 2c+9 (b2b3)
+      uint32_t bw[2];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * c + 8 * half + e;
+          const int blk = k % NB;
+          const bool lo_part = (k / NB) == 1;
+          float cv = 0.f;
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb) cv = (bb == blk) ? csum[bb] : cv;
+          const float hi = __half2float(__float2half_rn(cv));
+          v[e] = k < 2 * NB ? (lo_part ? cv - hi : hi) : 0.f;
+        }
+        bw[half] = pack_half2(v[0], v[1]);
+      }
+      corrb[n][0] = bw[0];
+      corrb[n][1] = bw[1];
     }
   }
 
   float o[NT][2 * NB][4];
   float mt[NT][4];
+  float ones[kOnesMma ? NT : 1][kOnesMma ? NB : 1][4];
   float mrow[NT][2], lrow[NT][2];
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
 #pragma unroll
     for (int i = 0; i < 2 * NB; ++i) o[n][i][0] = o[n][i][1] = o[n][i][2] = o[n][i][3] = 0.f;
     mt[n][0] = mt[n][1] = mt[n][2] = mt[n][3] = 0.f;
+    if constexpr (kOnesMma) {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) ones[n][bb][0] = ones[n][bb][1] = ones[n][bb][2] = ones[n][bb][3] = 0.f;
+    }
     mrow[n][0] = mrow[n][1] = -INFINITY;
     lrow[n][0] = lrow[n][1] = 0.f;
   }
@@ -290,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
             if constexpr (kK8) {
-              float acc[4] = {cq[n][bb][0], cq[n][bb][1], cq[n][bb][0], cq[n][bb][1]};
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
               mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
               mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
               const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
@@ -305,57 +339,94 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
             }
           }
         }
+        if constexpr (kK8) {
+          // bias removal: A[token][k] = d of block k % nb (k < 2nb), B = corrb
+          uint32_t ad[4];
+          if constexpr (NB == 4) {
+            ad[0] = (c & 1) ? dk0[1] : dk0[0];
+            ad[1] = (c & 1) ? dk1[1] : dk1[0];
+            ad[2] = 0u;
+            ad[3] = 0u;
+          } else {
+            const uint32_t x0 = c == 0 ? dk0[0] : c == 1 ? dk0[1] : c == 2 ? dk0[2] : dk0[3];
+            const uint32_t x1 = c == 0 ? dk1[0] : c == 1 ? dk1[1] : c == 2 ? dk1[2] : dk1[3];
+            ad[0] = x0;
+            ad[1] = x1;
+            ad[2] = x0;
+            ad[3] = x1;
+          }
+#pragma unroll
+          for (int n = 0; n < NT; ++n) mma_16816(sc[n], ad, corrb[n][0], corrb[n][1]);
+        }
       }
 
       // ------------------------------------------------- online softmax --
       uint32_t pb[NT][2];
-      float alpha[NT][2];
-      bool same = true;
+      float s4[NT][4];
+      bool grow = false;      // some row's maximum passed its reference by more than kLazy
+      float mx[NT][2];
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        float s4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s4[e] = sc[n][e] * p.scale_log2;
+        for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
         if (masked) {
           const int t0 = pos0 + g, t1 = pos0 + g + 8;
-          s4[0] = t0 <= lastv[n][0] ? s4[0] : -INFINITY;
-          s4[1] = t0 <= lastv[n][1] ? s4[1] : -INFINITY;
-          s4[2] = t1 <= lastv[n][0] ? s4[2] : -INFINITY;
-          s4[3] = t1 <= lastv[n][1] ? s4[3] : -INFINITY;
+          s4[n][0] = t0 <= lastv[n][0] ? s4[n][0] : -INFINITY;
+          s4[n][1] = t0 <= lastv[n][1] ? s4[n][1] : -INFINITY;
+          s4[n][2] = t1 <= lastv[n][0] ? s4[n][2] : -INFINITY;
+          s4[n][3] = t1 <= lastv[n][1] ? s4[n][3] : -INFINITY;
         }
-        float p4[4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          float mx = fmaxf(s4[u], s4[2 + u]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(mrow[n][u], mx);
-          same = same && (mnew == mrow[n][u]);
-          const float muse = mnew == -INFINITY ? 0.f : mnew;
-          alpha[n][u] = fast_exp2(mrow[n][u] - muse);
-          p4[u] = fast_exp2(s4[u] - muse);
-          p4[2 + u] = fast_exp2(s4[2 + u] - muse);
-          lrow[n][u] = fmaf(lrow[n][u], alpha[n][u], p4[u] + p4[2 + u]);
-          mrow[n][u] = mnew;
+          float m1 = fmaxf(s4[n][u], s4[n][2 + u]);
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 8));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
+          mx[n][u] = m1;
+          grow = grow || (m1 > mrow[n][u] + kLazy);
         }
-        pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
-        pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
       }
-      // the running maxima rarely move once a few pages are in: rescale only when one did
-      if (!__all_sync(0xffffffffu, same)) {
+      // The reference maximum of a row moves only when a score exceeds it by
+      // more than kLazy (log2 units): until then the weights stay <= 4, and O
+      // and l need no rescale.  4 keeps P * d (the V operand, d <= 65504/7)
+      // finite in fp16 for any finite input.  Warp-uniform decision.
+      if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
+            const float mnew = fmaxf(mrow[n][u], mx[n][u]);
+            const float alpha = mnew == -INFINITY ? 1.f : fast_exp2(mrow[n][u] - mnew);
+            mrow[n][u] = mnew;
+            lrow[n][u] *= alpha;
 #pragma unroll
             for (int i2 = 0; i2 < 2 * NB; ++i2) {
-              o[n][i2][u] *= alpha[n][u];
-              o[n][i2][2 + u] *= alpha[n][u];
+              o[n][i2][u] *= alpha;
+              o[n][i2][2 + u] *= alpha;
             }
-            if constexpr (kQ5) mt[n][u] *= alpha[n][u];
+            if constexpr (kQ5) mt[n][u] *= alpha;
+            if constexpr (kOnesMma) {
+#pragma unroll
+              for (int bb = 0; bb < NB; ++bb) {
+                ones[n][bb][u] *= alpha;
+                ones[n][bb][2 + u] *= alpha;
+              }
+            }
           }
         }
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        float p4[4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float muse = mrow[n][u] == -INFINITY ? 0.f : mrow[n][u];
+          p4[u] = fast_exp2(s4[n][u] - muse);
+          p4[2 + u] = fast_exp2(s4[n][2 + u] - muse);
+          lrow[n][u] += p4[u] + p4[2 + u];
+        }
+        pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
+        pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
       }
 
       // ---------------------------------------------- O^T += V^ P^T ---------
@@ -404,23 +475,39 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
             for (int n = 0; n < NT; ++n) {
               bs[n][0] = hmul2_u32(pb[n][0], dv[bb].x);
               bs[n][1] = hmul2_u32(pb[n][1], dv[bb].y);
+              if constexpr (kOnesMma) mma_16816(ones[n][bb], kOnesA, bs[n][0], bs[n][1]);
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t w = bh == 0 ? (h == 0 ? nw.x : nw.y) : (h == 0 ? nw.z : nw.w);
+              // Pairs 0 and 2 (dim slot g) become 1024 + code, pairs 1 and 3 (slot
+              // g+8) 1024 + 16 code: nibbles spliced under the exponent of 1024,
+              // the odd pairs without a shift.
+              const uint32_t w8 = w >> 8;
               uint32_t a[4];
-#pragma unroll
-              for (int ii = 0; ii < 4; ++ii) {
-                uint32_t t = ((w >> (4 * ii)) & 0x000F000Fu) | 0x64006400u;
-                if constexpr (kQ5) {
-                  // bit 4 of the pair's codes sits at 8p + 4(bb%2) + 2h + s (+16 for the second token)
-                  const int sh = 8 * (ii >> 1) + 4 * bh + 2 * h + (ii & 1) - 4;
-                  const uint32_t x = sh >= 0 ? (hw[bp] >> sh) : (hw[bp] << (-sh));
-                  t |= x & 0x00100010u;
-                  a[ii] = hsub2_u32(t, 0x64006400u);
-                } else {
-                  a[ii] = hsub2_u32(t, 0x64086408u);
-                }
+              a[0] = (w & 0x000F000Fu) | 0x64006400u;
+              a[1] = (w & 0x00F000F0u) | 0x64006400u;
+              a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+              a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+              if constexpr (kQ5) {
+                // bit 4 of the codes of nibble word k = 2*(bb%2) + h sits at
+                // 4s + 16f + k + 8p of the block pair's word: two shifts place
+                // it at 16 (pairs 0, 2) or 256 (pairs 1, 3) of the fp16 value.
+                const int k = 2 * bh + h;
+                const uint32_t x0 = hw[bp] << (4 - k);
+                const uint32_t x1 = hw[bp] >> (4 + k);
+                a[0] |= x0 & 0x00100010u;
+                a[1] |= x0 & 0x01000100u;
+                a[2] |= x1 & 0x00100010u;
+                a[3] |= x1 & 0x01000100u;
+              }
+              if constexpr (!kOnesMma) {
+                constexpr uint32_t kSub0 = kQ5 ? 0x64006400u : 0x64086408u;      // 1024 | 1032
+                constexpr uint32_t kSub1 = kQ5 ? 0xD400D400u : 0xD480D480u;      // -64 | -72
+                a[0] = hsub2_u32(a[0], kSub0);
+                a[2] = hsub2_u32(a[2], kSub0);
+                a[1] = hfma2_u32(a[1], 0x2C002C00u, kSub1);                      // x / 16 + (-64 | -72)
+                a[3] = hfma2_u32(a[3], 0x2C002C00u, kSub1);
               }
 #pragma unroll
               for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, bs[n][0], bs[n][1]);
@@ -469,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
       if (issuer && i + NS < npages) {
         if (mbar_wait_bounded(empty0 + 8 * s, par, p.status)) {
           fence_proxy_async();
-          issue(i + NS);
+          issue(i + NS, s);
         }
       }
     }
@@ -497,6 +584,25 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       lrow[n][u] = l;
+    }
+  }
+  if constexpr (kOnesMma) {
+    // remove the fp16 code offsets: slot g holds sum B (1024 + code) (+8 for
+    // q4_0's stored code), slot g+8 sum B (1024 + 16 stored code)
+    constexpr float kOff0 = kQ5 ? 1024.f : 1032.f, kOff1 = kQ5 ? 1024.f : 1152.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float *v = o[n][2 * bb + h];
+          v[0] = fmaf(-kOff0, ones[n][bb][0], v[0]);
+          v[1] = fmaf(-kOff0, ones[n][bb][1], v[1]);
+          v[2] = fmaf(-kOff1, ones[n][bb][0], v[2]) * 0.0625f;
+          v[3] = fmaf(-kOff1, ones[n][bb][1], v[3]) * 0.0625f;
+        }
+      }
     }
   }
   __syncthreads();                       // every warp is done with the ring

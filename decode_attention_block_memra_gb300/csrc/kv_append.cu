@@ -219,23 +219,26 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
         }
       }
       if (p.v_fmt == MEMRA_KV_Q5_1) {
-        // bit 4 of each code: per vg a 4-bit group (bit 2h+s); blocks 2bp and
-        // 2bp+1 share a byte, so the even block's lane gathers its partner's.
+        // bit 4 of each code: the byte of (vg, token) holds bit 4*s + 2*(b%2) + h,
+        // so the even block's lane merges its partner's bits (shifted by 2).
         uint32_t hn[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           hn[u] = 0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) hn[u] |= static_cast<uint32_t>((q[4 * u + e] >> 4) & 1) << e;
+          for (int e = 0; e < 4; ++e) {
+            const int h = e / 2, s = e % 2;
+            hn[u] |= static_cast<uint32_t>((q[4 * u + e] >> 4) & 1) << (4 * s + h);
+          }
         }
-        const uint32_t mine = hn[0] | (hn[1] << 4);
+        const uint32_t mine = hn[0] | (hn[1] << 8);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 4);   // lane of block b^1
         if (act && (b % 2) == 0) {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int vg = 2 * cc + u;
-            const uint32_t lo = (mine >> (4 * u)) & 15u, hi = (other >> (4 * u)) & 15u;
-            seg[8 * D + ((4 * vg + c) * (kNb / 2) + b / 2) * 4 + k] = static_cast<uint8_t>(lo | (hi << 4));
+            const uint32_t lo = (mine >> (8 * u)) & 0x33u, hi = (other >> (8 * u)) & 0x33u;
+            seg[8 * D + ((4 * vg + c) * (kNb / 2) + b / 2) * 4 + k] = static_cast<uint8_t>(lo | (hi << 2));
           }
         }
       }

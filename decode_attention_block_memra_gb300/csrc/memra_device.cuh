@@ -150,6 +150,12 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b),
+                      *reinterpret_cast<__half2 *>(&c));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);

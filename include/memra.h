@@ -56,7 +56,7 @@
  *      lane = 4*vg + c, k = 2*f + p
  *   V q5_1 / q4_0 low nibble (q5_1: q & 15; q4_0: q + 8):
  *       byte ((b/2)*32 + lane)*16 + (b%2)*8 + 4*h + k, bits 4*s .. 4*s+3
- *   V q5_1 bit 4 of q: byte 8*D + (lane*(nb/2) + b/2)*4 + k, bit 4*(b%2)+2*h+s
+ *   V q5_1 bit 4 of q: byte 8*D + (lane*(nb/2) + b/2)*4 + k, bit 4*s + 2*(b%2) + h
  *   V q5_1 d: 10*D + ((c*nb + b)*4 + 2*p + f)*2,  m: 11*D + same offset
  *   V q4_0 d: 8*D + ((c*nb + b)*4 + 2*p + f)*2
  *   V fp8:    byte (b*32 + lane)*16 + 8*h + 2*(2*p + s) + f

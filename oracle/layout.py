@@ -22,7 +22,7 @@ V side
     c = (t % 8) // 2, f = t % 2, p = t // 8, lane = 4 vg + c, k = 2 f + p
     nibble      byte ((b//2) 32 + lane) 16 + (b%2) 8 + 4 h + k, bits 4s..4s+3
                 (q5_1: the low 4 bits of q; q4_0: q + 8)
-    q5_1 bit 4  byte 8 D + (lane (nb/2) + b//2) 4 + k, bit 4 (b%2) + 2 h + s
+    q5_1 bit 4  byte 8 D + (lane (nb/2) + b//2) 4 + k, bit 4 s + 2 (b%2) + h
     q5_1 d, m   10 D (d) / 11 D (m) + ((c nb + b) 4 + 2 p + f) 2
     q4_0 d      8 D + ((c nb + b) 4 + 2 p + f) 2
     fp8 byte    (b 32 + lane) 16 + 8 h + 2 (2 p + s) + f
@@ -91,7 +91,7 @@ def v_hibit_offset(t, j, D):
     """(byte, bit) of bit 4 of a q5_1 code."""
     nb = D // 32
     b, vg, h, s, c, f, p, lane, k = _v_coords(t, j)
-    return 8 * D + (lane * (nb // 2) + b // 2) * 4 + k, 4 * (b % 2) + 2 * h + s
+    return 8 * D + (lane * (nb // 2) + b // 2) * 4 + k, 4 * s + 2 * (b % 2) + h
 
 
 def v_param_offset(t, b, D, base):

@@ -63,8 +63,8 @@ def test_q5_1_high_bit_and_nibble_split():
     layout.write_rows(pool, "v", f, np.array([11]), 0, D)
     seg = pool[0, 0]
     assert seg[723] == 0xB0            # t=11, j=77: nibble byte 723, upper nibble
-    assert seg[1135] == 0x02           # bit-4 byte 1135, bit 1
-    assert seg[:1024].sum() == 0xB0 and seg[1024:1280].sum() == 0x02
+    assert seg[1135] == 0x10           # bit-4 byte 1135, bit 4
+    assert seg[:1024].sum() == 0xB0 and seg[1024:1280].sum() == 0x10
 
 
 def golden_rows():
