@@ -234,7 +234,7 @@ def run_reference_arm(args) -> None:
 def workload_config(w) -> dict:
     return {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "context_tokens": int(w.seq_lens.sum()), "unique_tokens": int(w.slots.size),
-            "kv_format": f"{w.k_fmt}/{w.v_fmt}", "page_size": 16, "split_tokens": 1024,
+            "kv_format": f"{w.k_fmt}/{w.v_fmt}", "page_size": 16, "split_tokens": "max(1024, T / (SMs x CTAs per SM / KV heads))",
             "l2": "flushed between steps (256 MiB write outside the timed events)"}
 
 
@@ -244,6 +244,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--formats", default=None, help="K/V formats overriding the workload's, e.g. q8_0/q4_0")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-reps", type=int, default=5)
@@ -276,6 +277,8 @@ def main():
     _build.build()
     memra.lib()
     w = W.WORKLOADS[args.workload]()
+    if args.formats:
+        w = w.with_formats(*args.formats.split("/"))
     dw = upload(w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")

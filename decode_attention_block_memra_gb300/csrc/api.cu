@@ -36,9 +36,28 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MEMRA_OK : MEMRA_ERR_
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
-  int nt, ngrp, qg, nsplit_max, num_stages;
+  int nt, ngrp, qg, nsplit_max, num_stages, ctas_per_sm;
   size_t smem;
 };
+
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Splits one long sequence gets per KV head: one wave of the GPU.
+int split_target(const Plan &pl, int n_kv_heads) {
+  const int t = device_sms() * pl.ctas_per_sm / (n_kv_heads > 0 ? n_kv_heads : 1);
+  return t > 0 ? t : 1;
+}
 
 size_t merge_bytes(int D, int nt) {
   const size_t rows_w = 8 * nt, nb = D / 32;
@@ -80,7 +99,8 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   pl->qg = qg;
   pl->nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
   pl->num_stages = ns;
-  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(kSplitPages);
+  pl->ctas_per_sm = ctas_per_sm;
+  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(kSplitPagesMax);
   return MEMRA_OK;
 }
 
@@ -157,6 +177,7 @@ int run_partials(const DecodeArgs &a, cudaStream_t st) {
   p.nsplit_max = pl.nsplit_max;
   p.num_stages = pl.num_stages;
   p.ngrp = pl.ngrp;
+  p.split_target = split_target(pl, c.n_kv_heads);
   const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
@@ -188,6 +209,10 @@ int run_combine(const memra_kv_cache *c, const int32_t *seq_lens, int32_t max_se
   p.max_seq_len = max_seq_len;
   p.max_pages = max_pages;
   p.nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
+  Plan pl;
+  int rc = make_plan(head_dim, c->k_fmt, c->v_fmt, q_len, n_heads / c->n_kv_heads, max_seq_len, &pl);
+  if (rc) return rc;
+  p.split_target = split_target(pl, c->n_kv_heads);
   return cuda_status(launch_combine(head_dim, p, st));
 }
 
@@ -244,7 +269,7 @@ int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_le
   int st = check_cache(cache);
   if (st) return st;
   if (batch < 0 || q_len < 1 || n_heads < 1 || max_seq_len < 0 || head_dim != cache->head_dim ||
-      max_pages_per_seq < 0)
+      max_pages_per_seq < 0 || n_heads % cache->n_kv_heads)
     return MEMRA_ERR_INVALID_ARG;
   if (batch == 0) return MEMRA_OK;
   if (!seq_lens || !out || !aligned16(out)) return MEMRA_ERR_INVALID_ARG;

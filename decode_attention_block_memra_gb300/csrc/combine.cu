@@ -1,6 +1,6 @@
 // K3: log-sum-exp combine of the split-K partials.
 //
-// For a query row whose sequence spans several 1024-token splits, the split
+// For a query row whose sequence spans several splits, the split
 // kernel left (o_s = O_s / l_s, lse_s = m_s + log2 l_s) per split.  The exact
 // merge is  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max lse_s
 // (splits with no visible key have lse = -inf and weight 0).  One CTA per
@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
   const int nw = blockDim.x >> 5;
   const int b = row / (p.q_len * p.n_heads);
   const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status, false);
-  const int ns = (T + kSplitTokens - 1) / kSplitTokens;
+  const int C = split_tokens(T, p.split_target);
+  const int ns = (T + C - 1) / C;
   if (ns == 1) return;                              // the split kernel wrote this row
   __half *dst = p.out + static_cast<size_t>(row) * D;
   if (ns == 0) {                                    // empty sequence: zeros

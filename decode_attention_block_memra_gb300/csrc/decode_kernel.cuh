@@ -1,6 +1,6 @@
 // K2: split-K flash-decoding over the block-quantized paged KV cache.
 //
-// What it computes: for one (sequence, KV head, split of 1024 tokens), the
+// What it computes: for one (sequence, KV head, split of C(T) tokens), the
 // partial softmax(q K^T * scale) V over the split's keys for all the query
 // rows that read this KV head (the head's GQA group times q_len, causal among
 // the q_len new tokens), as (o = O / l, lse = m + log2 l).  The KV formats are
@@ -46,7 +46,7 @@ struct DecodeParams {
   float *lse_part;    // [rows][nsplit_max]
   int32_t *status;
   int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group, qg;
-  int nsplit_max, num_stages, ngrp;
+  int nsplit_max, num_stages, ngrp, split_target;
   float scale_log2, v_scale;
 };
 
@@ -56,7 +56,7 @@ struct CombineParams {
   const float *lse_part;
   __half *out;
   int32_t *status;
-  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max;
+  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max, split_target;
 };
 
 cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
@@ -129,10 +129,11 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status,
                               split == 0 && kvh == 0 && threadIdx.x == 0);
-  const int tok0 = split * kSplitTokens;
+  const int C = split_tokens(T, p.split_target);
+  const int tok0 = split * C;
   if (tok0 >= T) return;
-  const int npages = (min(T, tok0 + kSplitTokens) - tok0 + kPage - 1) / kPage;
-  const int nsplit_b = (T + kSplitTokens - 1) / kSplitTokens;
+  const int npages = (min(T, tok0 + C) - tok0 + kPage - 1) / kPage;
+  const int nsplit_b = (T + C - 1) / C;
 
   const int NS = p.num_stages;                  // a multiple of 4, so page i and i + NS share a warp
   const int region = max(NS * STAGE, ML::kBytes);

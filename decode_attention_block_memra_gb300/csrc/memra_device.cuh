@@ -13,8 +13,19 @@
 namespace memra {
 
 constexpr int kPage = MEMRA_PAGE_SIZE;
-constexpr int kSplitTokens = MEMRA_SPLIT_TOKENS;
-constexpr int kSplitPages = kSplitTokens / kPage;
+constexpr int kSplitTokens = MEMRA_SPLIT_TOKENS;            // smallest split
+constexpr int kSplitTokensMax = MEMRA_SPLIT_TOKENS_MAX;      // largest split
+constexpr int kSplitPagesMax = kSplitTokensMax / kPage;
+
+// Split size of a sequence of T tokens: enough splits to give one long
+// sequence `target` CTAs per KV head, never below 1024 or above 8192 tokens,
+// a multiple of the page.  Depends on T and the device only.
+__host__ __device__ __forceinline__ int split_tokens(int T, int target) {
+  const int t = target > 0 ? target : 1;
+  int c = (T + t - 1) / t;
+  c = (c + kPage - 1) / kPage * kPage;
+  return c < kSplitTokens ? kSplitTokens : (c > kSplitTokensMax ? kSplitTokensMax : c);
+}
 
 // Segment bytes per (format, side, head_dim); see the layout in memra.h.
 __host__ __device__ constexpr int k_seg_bytes(int fmt, int D) {

@@ -101,9 +101,16 @@ typedef enum {
     MEMRA_KV_FP8_E4M3 = 3    /* K or V */
 } memra_kv_format;
 
-/* Fixed page size (tokens) and the fixed token grid of the split-K plan. */
+/* Page size (tokens) and the bounds of the split-K plan.  A sequence of T
+ * tokens is cut into splits of C(T) tokens, C(T) = clamp(roundup16(ceil(T /
+ * S)), MEMRA_SPLIT_TOKENS, MEMRA_SPLIT_TOKENS_MAX), where S = (SMs of the
+ * device) x (CTAs per SM of the kernel configuration) / n_kv_heads, so that one
+ * long sequence fills the GPU in one wave.  C depends only on the sequence's
+ * own length and the device, never on the rest of the batch: a sequence's
+ * result bytes are the same alone or batched. */
 #define MEMRA_PAGE_SIZE 16
 #define MEMRA_SPLIT_TOKENS 1024
+#define MEMRA_SPLIT_TOKENS_MAX 8192
 
 /* A paged KV cache.  Plain data; the caller owns the pools and status word. */
 typedef struct {
@@ -142,7 +149,8 @@ int memra_kv_append(const memra_kv_cache *cache, const void *k, const void *v,
 
 /* Workspace bytes memra_decode_attn needs for these sizes (the split-K
  * partials: float32 [batch*q_len*n_heads][ceil(max_seq_len/1024)][head_dim]
- * plus one float32 log-sum-exp per partial).  Host only. */
+ * plus one float32 log-sum-exp per partial; ceil(max_seq_len/1024) bounds the
+ * split count of any sequence).  Host only. */
 size_t memra_decode_attn_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads,
                                          int32_t head_dim, int32_t max_seq_len);
 
@@ -211,7 +219,8 @@ int memra_read_status(const memra_kv_cache *cache, int32_t *flags, void *stream)
 /* Static English description of a memra_status value. */
 const char *memra_status_string(int status);
 
-/* Number of split-K partials a sequence of `seq_len` tokens produces. */
+/* Upper bound on the split-K partials of a sequence of `seq_len` tokens
+ * (ceil(seq_len / MEMRA_SPLIT_TOKENS)); the workspace is sized with it. */
 int32_t memra_num_splits(int32_t seq_len);
 
 #ifdef __cplusplus

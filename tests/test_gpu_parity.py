@@ -328,3 +328,12 @@ def test_adversarial_blocks_bit_exact(kf, vf):
     assert res.flags == 0
     assert_pools_exact(w, res)
     assert np.isfinite(res.out.astype(np.float32)).all()
+
+
+def test_long_sequence_with_wide_splits():
+    """A long sequence over many KV heads gets splits wider than 1,024 tokens (one wave per head)."""
+    w = W.make_workload("wide_splits", batch=2, q_len=2, n_heads=16, n_kv_heads=8, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=17, seq_lens=[100003, 57000], permute_pages=True)
+    res = run(w, want_pools=False)
+    assert res.flags == 0
+    assert_out_close(w, res, attention.reference(w))
