@@ -3,6 +3,7 @@
 // device memory or synchronizes, except memra_read_status.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -181,8 +182,10 @@ int run_partials(const DecodeArgs &a, cudaStream_t st) {
   const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
-  const dim3 grid(static_cast<unsigned>(pl.nsplit_max), static_cast<unsigned>(c.n_kv_heads),
-                  static_cast<unsigned>(a.batch));
+  // no sequence has more splits than min(ceil(T/1024), max(target, ceil(T/8192)))
+  const int64_t most = std::min<int64_t>(pl.nsplit_max, std::max<int64_t>(p.split_target,
+                                                                          ceil_div(a.max_seq_len, kSplitTokensMax)));
+  const dim3 grid(static_cast<unsigned>(most), static_cast<unsigned>(c.n_kv_heads), static_cast<unsigned>(a.batch));
   cudaError_t e;
   if (a.head_dim == 128)
     e = pl.nt == 1 ? launch_decode_d128_nt1(c.k_fmt, c.v_fmt, p, grid, pl.smem, st)

@@ -31,6 +31,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "memra_device.cuh"
 
 namespace memra {
@@ -285,277 +287,287 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
       break;
     }
     if (pid_s[i] >= 0) {
-      const uint32_t ka = ring + s * STAGE;
-      const uint32_t va = ka + KSEG;
-      const int pos0 = tok0 + i * kPage;
-      const bool masked = pos0 + kPage - 1 > min_last;
-      const bool partial = pos0 + kPage > T;
+      // Pages wholly inside every row's visible range (all but the last one or
+      // two of a sequence) take a path without any masking code.
+      const int pos_first = tok0 + i * kPage;
+      const bool plain = pos_first + kPage - 1 <= min_last && pos_first + kPage <= T;
+      auto page = [&](auto tail) {
+        const uint32_t ka = ring + s * STAGE;
+        const uint32_t va = ka + KSEG;
+        const int pos0 = tok0 + i * kPage;
+        constexpr bool masked = decltype(tail)::value;    // some key of the page is hidden from some row
+        constexpr bool partial = decltype(tail)::value;   // the page runs past the sequence
 
-      // ---------------------------------------------------- S^T = K^ Q^T --
-      float sc[NT][4];
+        // ---------------------------------------------------- S^T = K^ Q^T --
+        float sc[NT][4];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-      {
-        uint4 kc[NB];
+          for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+        {
+          uint4 kc[NB];
 #pragma unroll
-        for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
-        // q8_0 block scales of tokens g and g+8, two fp16 per word
-        uint32_t dk0[NB / 2], dk1[NB / 2];
-        if constexpr (kK8) {
-          if constexpr (NB == 4) {
-            const uint2 a = lds64(ka + 16 * D + g * NB * 2), bq = lds64(ka + 16 * D + (g + 8) * NB * 2);
-            dk0[0] = a.x; dk0[1] = a.y; dk1[0] = bq.x; dk1[1] = bq.y;
-          } else {
-            const uint4 a = lds128(ka + 16 * D + g * NB * 2), bq = lds128(ka + 16 * D + (g + 8) * NB * 2);
-            dk0[0] = a.x; dk0[1] = a.y; dk0[2] = a.z; dk0[3] = a.w;
-            dk1[0] = bq.x; dk1[1] = bq.y; dk1[2] = bq.z; dk1[3] = bq.w;
+            for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
+          // q8_0 block scales of tokens g and g+8, two fp16 per word
+          uint32_t dk0[NB / 2], dk1[NB / 2];
+          if constexpr (kK8) {
+            if constexpr (NB == 4) {
+              const uint2 a = lds64(ka + 16 * D + g * NB * 2), bq = lds64(ka + 16 * D + (g + 8) * NB * 2);
+              dk0[0] = a.x; dk0[1] = a.y; dk1[0] = bq.x; dk1[1] = bq.y;
+            } else {
+              const uint4 a = lds128(ka + 16 * D + g * NB * 2), bq = lds128(ka + 16 * D + (g + 8) * NB * 2);
+              dk0[0] = a.x; dk0[1] = a.y; dk0[2] = a.z; dk0[3] = a.w;
+              dk1[0] = bq.x; dk1[1] = bq.y; dk1[2] = bq.z; dk1[3] = bq.w;
+            }
+          }
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+            const uint4 &c0 = kc[bb / 2];
+            const uint4 &c1 = kc[NB / 2 + bb / 2];
+            const uint32_t t0lo = (bb & 1) ? c0.z : c0.x, t0hi = (bb & 1) ? c0.w : c0.y;
+            const uint32_t t1lo = (bb & 1) ? c1.z : c1.x, t1hi = (bb & 1) ? c1.w : c1.y;
+            uint32_t a0[4], a1[4];
+            k_pairs<KF>(t0lo, a0[0], a0[2]);
+            k_pairs<KF>(t1lo, a0[1], a0[3]);
+            k_pairs<KF>(t0hi, a1[0], a1[2]);
+            k_pairs<KF>(t1hi, a1[1], a1[3]);
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+              if constexpr (kK8) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
+                mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
+                const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
+                const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk1[bb / 2] >> (16 * (bb & 1)))));
+                sc[n][0] = fmaf(d0, acc[0], sc[n][0]);
+                sc[n][1] = fmaf(d0, acc[1], sc[n][1]);
+                sc[n][2] = fmaf(d1, acc[2], sc[n][2]);
+                sc[n][3] = fmaf(d1, acc[3], sc[n][3]);
+              } else {
+                mma_16816(sc[n], a0, qf[n][bb].x, qf[n][bb].y);
+                mma_16816(sc[n], a1, qf[n][bb].z, qf[n][bb].w);
+              }
+            }
+          }
+          if constexpr (kK8) {
+            // bias removal: A[token][k] = d of block k % nb (k < 2nb), B = corrb
+            uint32_t ad[4];
+            if constexpr (NB == 4) {
+              ad[0] = (c & 1) ? dk0[1] : dk0[0];
+              ad[1] = (c & 1) ? dk1[1] : dk1[0];
+              ad[2] = 0u;
+              ad[3] = 0u;
+            } else {
+              const uint32_t x0 = c == 0 ? dk0[0] : c == 1 ? dk0[1] : c == 2 ? dk0[2] : dk0[3];
+              const uint32_t x1 = c == 0 ? dk1[0] : c == 1 ? dk1[1] : c == 2 ? dk1[2] : dk1[3];
+              ad[0] = x0;
+              ad[1] = x1;
+              ad[2] = x0;
+              ad[3] = x1;
+            }
+#pragma unroll
+              for (int n = 0; n < NT; ++n) mma_16816(sc[n], ad, corrb[n][0], corrb[n][1]);
           }
         }
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) {
-          const uint4 &c0 = kc[bb / 2];
-          const uint4 &c1 = kc[NB / 2 + bb / 2];
-          const uint32_t t0lo = (bb & 1) ? c0.z : c0.x, t0hi = (bb & 1) ? c0.w : c0.y;
-          const uint32_t t1lo = (bb & 1) ? c1.z : c1.x, t1hi = (bb & 1) ? c1.w : c1.y;
-          uint32_t a0[4], a1[4];
-          k_pairs<KF>(t0lo, a0[0], a0[2]);
-          k_pairs<KF>(t1lo, a0[1], a0[3]);
-          k_pairs<KF>(t0hi, a1[0], a1[2]);
-          k_pairs<KF>(t1hi, a1[1], a1[3]);
+
+        // ------------------------------------------------- online softmax --
+        uint32_t pb[NT][2];
+        float s4[NT][4];
+        bool grow = false;      // some row's maximum passed its reference by more than kLazy
+        float mx[NT][2];
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
-            if constexpr (kK8) {
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
-              mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
-              const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
-              const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk1[bb / 2] >> (16 * (bb & 1)))));
-              sc[n][0] = fmaf(d0, acc[0], sc[n][0]);
-              sc[n][1] = fmaf(d0, acc[1], sc[n][1]);
-              sc[n][2] = fmaf(d1, acc[2], sc[n][2]);
-              sc[n][3] = fmaf(d1, acc[3], sc[n][3]);
-            } else {
-              mma_16816(sc[n], a0, qf[n][bb].x, qf[n][bb].y);
-              mma_16816(sc[n], a1, qf[n][bb].z, qf[n][bb].w);
-            }
-          }
-        }
-        if constexpr (kK8) {
-          // bias removal: A[token][k] = d of block k % nb (k < 2nb), B = corrb
-          uint32_t ad[4];
-          if constexpr (NB == 4) {
-            ad[0] = (c & 1) ? dk0[1] : dk0[0];
-            ad[1] = (c & 1) ? dk1[1] : dk1[0];
-            ad[2] = 0u;
-            ad[3] = 0u;
-          } else {
-            const uint32_t x0 = c == 0 ? dk0[0] : c == 1 ? dk0[1] : c == 2 ? dk0[2] : dk0[3];
-            const uint32_t x1 = c == 0 ? dk1[0] : c == 1 ? dk1[1] : c == 2 ? dk1[2] : dk1[3];
-            ad[0] = x0;
-            ad[1] = x1;
-            ad[2] = x0;
-            ad[3] = x1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
+          if (masked) {
+            const int t0 = pos0 + g, t1 = pos0 + g + 8;
+            s4[n][0] = t0 <= lastv[n][0] ? s4[n][0] : -INFINITY;
+            s4[n][1] = t0 <= lastv[n][1] ? s4[n][1] : -INFINITY;
+            s4[n][2] = t1 <= lastv[n][0] ? s4[n][2] : -INFINITY;
+            s4[n][3] = t1 <= lastv[n][1] ? s4[n][3] : -INFINITY;
           }
 #pragma unroll
-          for (int n = 0; n < NT; ++n) mma_16816(sc[n], ad, corrb[n][0], corrb[n][1]);
-        }
-      }
-
-      // ------------------------------------------------- online softmax --
-      uint32_t pb[NT][2];
-      float s4[NT][4];
-      bool grow = false;      // some row's maximum passed its reference by more than kLazy
-      float mx[NT][2];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
-        if (masked) {
-          const int t0 = pos0 + g, t1 = pos0 + g + 8;
-          s4[n][0] = t0 <= lastv[n][0] ? s4[n][0] : -INFINITY;
-          s4[n][1] = t0 <= lastv[n][1] ? s4[n][1] : -INFINITY;
-          s4[n][2] = t1 <= lastv[n][0] ? s4[n][2] : -INFINITY;
-          s4[n][3] = t1 <= lastv[n][1] ? s4[n][3] : -INFINITY;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float m1 = fmaxf(s4[n][u], s4[n][2 + u]);
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 8));
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
-          mx[n][u] = m1;
-          grow = grow || (m1 > mrow[n][u] + kLazy);
-        }
-      }
-      // The reference maximum of a row moves only when a score exceeds it by
-      // more than kLazy (log2 units): until then the weights stay <= 4, and O
-      // and l need no rescale.  4 keeps P * d (the V operand, d <= 65504/7)
-      // finite in fp16 for any finite input.  Warp-uniform decision.
-      if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float mnew = fmaxf(mrow[n][u], mx[n][u]);
-            const float alpha = mnew == -INFINITY ? 1.f : fast_exp2(mrow[n][u] - mnew);
-            mrow[n][u] = mnew;
-            lrow[n][u] *= alpha;
-#pragma unroll
-            for (int i2 = 0; i2 < 2 * NB; ++i2) {
-              o[n][i2][u] *= alpha;
-              o[n][i2][2 + u] *= alpha;
-            }
-            if constexpr (kQ5) mt[n][u] *= alpha;
-            if constexpr (kOnesMma) {
-#pragma unroll
-              for (int bb = 0; bb < NB; ++bb) {
-                ones[n][bb][u] *= alpha;
-                ones[n][bb][2 + u] *= alpha;
-              }
-            }
+            for (int u = 0; u < 2; ++u) {
+            float m1 = fmaxf(s4[n][u], s4[n][2 + u]);
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 8));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
+            mx[n][u] = m1;
+            grow = grow || (m1 > mrow[n][u] + kLazy);
           }
         }
-      }
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        float p4[4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float muse = mrow[n][u] == -INFINITY ? 0.f : mrow[n][u];
-          p4[u] = fast_exp2(s4[n][u] - muse);
-          p4[2 + u] = fast_exp2(s4[n][2 + u] - muse);
-          lrow[n][u] += p4[u] + p4[2 + u];
-        }
-        pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
-        pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
-      }
-
-      // ---------------------------------------------- O^T += V^ P^T ---------
-      // token-validity masks of the thread's B/A token pairs (partial pages only)
-      uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
-      if (partial) {
-        const int t = pos0 + 2 * c;
-        m01 = (t < T ? 0x0000FFFFu : 0u) | (t + 1 < T ? 0xFFFF0000u : 0u);
-        m89 = (t + 8 < T ? 0x0000FFFFu : 0u) | (t + 9 < T ? 0xFFFF0000u : 0u);
-      }
-      if constexpr (kVq) {
-        constexpr int DOFF = kQ5 ? 10 * D : 8 * D;
-        uint2 dv[NB];
-#pragma unroll
-        for (int q2 = 0; q2 < NB / 2; ++q2) {
-          const uint4 x = lds128(va + DOFF + c * NB * 8 + q2 * 16);
-          dv[2 * q2] = make_uint2(x.x, x.y);
-          dv[2 * q2 + 1] = make_uint2(x.z, x.w);
-        }
-        if (partial) {
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb) {
-            dv[bb].x &= m01;
-            dv[bb].y &= m89;
-          }
-        }
-        uint32_t hw[NB / 2];
-        if constexpr (kQ5) {
-          if constexpr (NB == 4) {
-            const uint2 x = lds64(va + 8 * D + lane * (NB / 2) * 4);
-            hw[0] = x.x;
-            hw[1] = x.y;
-          } else {
-            const uint4 x = lds128(va + 8 * D + lane * (NB / 2) * 4);
-            hw[0] = x.x; hw[1] = x.y; hw[2] = x.z; hw[3] = x.w;
-          }
-        }
-#pragma unroll
-        for (int bp = 0; bp < NB / 2; ++bp) {
-          const uint4 nw = lds128(va + (bp * 32 + lane) * 16);
-#pragma unroll
-          for (int bh = 0; bh < 2; ++bh) {
-            const int bb = 2 * bp + bh;
-            uint32_t bs[NT][2];
+        // The reference maximum of a row moves only when a score exceeds it by
+        // more than kLazy (log2 units): until then the weights stay <= 4, and O
+        // and l need no rescale.  4 keeps P * d (the V operand, d <= 65504/7)
+        // finite in fp16 for any finite input.  Warp-uniform decision.
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-              bs[n][0] = hmul2_u32(pb[n][0], dv[bb].x);
-              bs[n][1] = hmul2_u32(pb[n][1], dv[bb].y);
-              if constexpr (kOnesMma) mma_16816(ones[n][bb], kOnesA, bs[n][0], bs[n][1]);
-            }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t w = bh == 0 ? (h == 0 ? nw.x : nw.y) : (h == 0 ? nw.z : nw.w);
-              // Pairs 0 and 2 (dim slot g) become 1024 + code, pairs 1 and 3 (slot
-              // g+8) 1024 + 16 code: nibbles spliced under the exponent of 1024,
-              // the odd pairs without a shift.
-              const uint32_t w8 = w >> 8;
+              for (int u = 0; u < 2; ++u) {
+              const float mnew = fmaxf(mrow[n][u], mx[n][u]);
+              const float alpha = mnew == -INFINITY ? 1.f : fast_exp2(mrow[n][u] - mnew);
+              mrow[n][u] = mnew;
+              lrow[n][u] *= alpha;
+#pragma unroll
+                for (int i2 = 0; i2 < 2 * NB; ++i2) {
+                o[n][i2][u] *= alpha;
+                o[n][i2][2 + u] *= alpha;
+              }
+              if constexpr (kQ5) mt[n][u] *= alpha;
+              if constexpr (kOnesMma) {
+#pragma unroll
+                  for (int bb = 0; bb < NB; ++bb) {
+                  ones[n][bb][u] *= alpha;
+                  ones[n][bb][2 + u] *= alpha;
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+          float p4[4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+            const float muse = mrow[n][u] == -INFINITY ? 0.f : mrow[n][u];
+            p4[u] = fast_exp2(s4[n][u] - muse);
+            p4[2 + u] = fast_exp2(s4[n][2 + u] - muse);
+            lrow[n][u] += p4[u] + p4[2 + u];
+          }
+          pb[n][0] = movmatrix_trans(pack_half2(p4[0], p4[1]));   // tokens 2c, 2c+1 of row g
+          pb[n][1] = movmatrix_trans(pack_half2(p4[2], p4[3]));   // tokens 2c+8, 2c+9
+        }
+
+        // ---------------------------------------------- O^T += V^ P^T ---------
+        // token-validity masks of the thread's B/A token pairs (partial pages only)
+        uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+        if (partial) {
+          const int t = pos0 + 2 * c;
+          m01 = (t < T ? 0x0000FFFFu : 0u) | (t + 1 < T ? 0xFFFF0000u : 0u);
+          m89 = (t + 8 < T ? 0x0000FFFFu : 0u) | (t + 9 < T ? 0xFFFF0000u : 0u);
+        }
+        if constexpr (kVq) {
+          constexpr int DOFF = kQ5 ? 10 * D : 8 * D;
+          uint2 dv[NB];
+#pragma unroll
+            for (int q2 = 0; q2 < NB / 2; ++q2) {
+            const uint4 x = lds128(va + DOFF + c * NB * 8 + q2 * 16);
+            dv[2 * q2] = make_uint2(x.x, x.y);
+            dv[2 * q2 + 1] = make_uint2(x.z, x.w);
+          }
+          if (partial) {
+#pragma unroll
+              for (int bb = 0; bb < NB; ++bb) {
+              dv[bb].x &= m01;
+              dv[bb].y &= m89;
+            }
+          }
+          uint32_t hw[NB / 2];
+          if constexpr (kQ5) {
+            if constexpr (NB == 4) {
+              const uint2 x = lds64(va + 8 * D + lane * (NB / 2) * 4);
+              hw[0] = x.x;
+              hw[1] = x.y;
+            } else {
+              const uint4 x = lds128(va + 8 * D + lane * (NB / 2) * 4);
+              hw[0] = x.x; hw[1] = x.y; hw[2] = x.z; hw[3] = x.w;
+            }
+          }
+#pragma unroll
+            for (int bp = 0; bp < NB / 2; ++bp) {
+            const uint4 nw = lds128(va + (bp * 32 + lane) * 16);
+#pragma unroll
+              for (int bh = 0; bh < 2; ++bh) {
+              const int bb = 2 * bp + bh;
+              uint32_t bs[NT][2];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                bs[n][0] = hmul2_u32(pb[n][0], dv[bb].x);
+                bs[n][1] = hmul2_u32(pb[n][1], dv[bb].y);
+                if constexpr (kOnesMma) mma_16816(ones[n][bb], kOnesA, bs[n][0], bs[n][1]);
+              }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                const uint32_t w = bh == 0 ? (h == 0 ? nw.x : nw.y) : (h == 0 ? nw.z : nw.w);
+                // Pairs 0 and 2 (dim slot g) become 1024 + code, pairs 1 and 3 (slot
+                // g+8) 1024 + 16 code: nibbles spliced under the exponent of 1024,
+                // the odd pairs without a shift.
+                const uint32_t w8 = w >> 8;
+                uint32_t a[4];
+                a[0] = (w & 0x000F000Fu) | 0x64006400u;
+                a[1] = (w & 0x00F000F0u) | 0x64006400u;
+                a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+                a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+                if constexpr (kQ5) {
+                  // bit 4 of the codes of nibble word k = 2*(bb%2) + h sits at
+                  // 4s + 16f + k + 8p of the block pair's word: two shifts place
+                  // it at 16 (pairs 0, 2) or 256 (pairs 1, 3) of the fp16 value.
+                  const int k = 2 * bh + h;
+                  const uint32_t x0 = hw[bp] << (4 - k);
+                  const uint32_t x1 = hw[bp] >> (4 + k);
+                  a[0] |= x0 & 0x00100010u;
+                  a[1] |= x0 & 0x01000100u;
+                  a[2] |= x1 & 0x00100010u;
+                  a[3] |= x1 & 0x01000100u;
+                }
+                if constexpr (!kOnesMma) {
+                  constexpr uint32_t kSub0 = kQ5 ? 0x64006400u : 0x64086408u;      // 1024 | 1032
+                  constexpr uint32_t kSub1 = kQ5 ? 0xD400D400u : 0xD480D480u;      // -64 | -72
+                  a[0] = hsub2_u32(a[0], kSub0);
+                  a[2] = hsub2_u32(a[2], kSub0);
+                  a[1] = hfma2_u32(a[1], 0x2C002C00u, kSub1);                      // x / 16 + (-64 | -72)
+                  a[3] = hfma2_u32(a[3], 0x2C002C00u, kSub1);
+                }
+#pragma unroll
+                  for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, bs[n][0], bs[n][1]);
+              }
+            }
+          }
+          if constexpr (kQ5) {
+            uint2 mv = make_uint2(0, 0);
+            if (g < NB) {
+              mv = lds64(va + 11 * D + (c * NB + g) * 8);
+              if (partial) {
+                mv.x &= m01;
+                mv.y &= m89;
+              }
+            }
+            const uint32_t am[4] = {mv.x, 0u, mv.y, 0u};
+#pragma unroll
+              for (int n = 0; n < NT; ++n) mma_16816(mt[n], am, pb[n][0], pb[n][1]);
+          }
+        } else {  // fp8 V
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+            const uint4 x = lds128(va + (bb * 32 + lane) * 16);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+              const uint32_t w0 = h == 0 ? x.x : x.z, w1 = h == 0 ? x.y : x.w;
               uint32_t a[4];
-              a[0] = (w & 0x000F000Fu) | 0x64006400u;
-              a[1] = (w & 0x00F000F0u) | 0x64006400u;
-              a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-              a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
-              if constexpr (kQ5) {
-                // bit 4 of the codes of nibble word k = 2*(bb%2) + h sits at
-                // 4s + 16f + k + 8p of the block pair's word: two shifts place
-                // it at 16 (pairs 0, 2) or 256 (pairs 1, 3) of the fp16 value.
-                const int k = 2 * bh + h;
-                const uint32_t x0 = hw[bp] << (4 - k);
-                const uint32_t x1 = hw[bp] >> (4 + k);
-                a[0] |= x0 & 0x00100010u;
-                a[1] |= x0 & 0x01000100u;
-                a[2] |= x1 & 0x00100010u;
-                a[3] |= x1 & 0x01000100u;
-              }
-              if constexpr (!kOnesMma) {
-                constexpr uint32_t kSub0 = kQ5 ? 0x64006400u : 0x64086408u;      // 1024 | 1032
-                constexpr uint32_t kSub1 = kQ5 ? 0xD400D400u : 0xD480D480u;      // -64 | -72
-                a[0] = hsub2_u32(a[0], kSub0);
-                a[2] = hsub2_u32(a[2], kSub0);
-                a[1] = hfma2_u32(a[1], 0x2C002C00u, kSub1);                      // x / 16 + (-64 | -72)
-                a[3] = hfma2_u32(a[3], 0x2C002C00u, kSub1);
+              a[0] = e4m3x2_to_half2(w0 & 0xFFFFu);
+              a[1] = e4m3x2_to_half2(w0 >> 16);
+              a[2] = e4m3x2_to_half2(w1 & 0xFFFFu);
+              a[3] = e4m3x2_to_half2(w1 >> 16);
+              if (partial) {
+                a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
               }
 #pragma unroll
-              for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, bs[n][0], bs[n][1]);
+                for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, pb[n][0], pb[n][1]);
             }
           }
         }
-        if constexpr (kQ5) {
-          uint2 mv = make_uint2(0, 0);
-          if (g < NB) {
-            mv = lds64(va + 11 * D + (c * NB + g) * 8);
-            if (partial) {
-              mv.x &= m01;
-              mv.y &= m89;
-            }
-          }
-          const uint32_t am[4] = {mv.x, 0u, mv.y, 0u};
-#pragma unroll
-          for (int n = 0; n < NT; ++n) mma_16816(mt[n], am, pb[n][0], pb[n][1]);
-        }
-      } else {  // fp8 V
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) {
-          const uint4 x = lds128(va + (bb * 32 + lane) * 16);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t w0 = h == 0 ? x.x : x.z, w1 = h == 0 ? x.y : x.w;
-            uint32_t a[4];
-            a[0] = e4m3x2_to_half2(w0 & 0xFFFFu);
-            a[1] = e4m3x2_to_half2(w0 >> 16);
-            a[2] = e4m3x2_to_half2(w1 & 0xFFFFu);
-            a[3] = e4m3x2_to_half2(w1 >> 16);
-            if (partial) {
-              a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
-            }
-#pragma unroll
-            for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, pb[n][0], pb[n][1]);
-          }
-        }
-      }
+          };
+      if (plain)
+        page(std::false_type{});
+      else
+        page(std::true_type{});
     }
     __syncwarp();
     // Release the stage; the page lane's issuing warp refills it with page i + NS
     // once every row group has released it.
     if (lane == 0) {
-      mbar_arrive(empty0 + 8 * s);
+      if (ngrp > 1) mbar_arrive(empty0 + 8 * s);       // other row groups read this stage too
       if (issuer && i + NS < npages) {
-        if (mbar_wait_bounded(empty0 + 8 * s, par, p.status)) {
+        if (ngrp == 1 || mbar_wait_bounded(empty0 + 8 * s, par, p.status)) {
           fence_proxy_async();
           issue(i + NS, s);
         }
