@@ -12,7 +12,8 @@ permutation of the pool).
 Prints one JSON line (rank 0).  value = query tokens per second of the whole
 job (decode-attention throughput); kv_gbs = unique quantized-KV bytes per
 second.  Timing: CUDA events on the launching stream around every step, an
-L2 flush (256 MiB write) between steps outside the events, max over ranks.
+L2 flush (256 MiB write, then read back so no dirty line is left) between
+steps outside the events, max over ranks.
 With --gpus N (under torchrun) every rank runs an independent replica of the
 workload (the path shards into independent sequences; there is no exchange).
 """
@@ -235,7 +236,7 @@ def workload_config(w) -> dict:
     return {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "context_tokens": int(w.seq_lens.sum()), "unique_tokens": int(w.slots.size),
             "kv_format": f"{w.k_fmt}/{w.v_fmt}", "page_size": 16, "split_tokens": "max(1024, T / (SMs x CTAs per SM / KV heads))",
-            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+            "l2": "flushed between steps (256 MiB write, then read back, outside the timed events)"}
 
 
 def main():
@@ -282,6 +283,13 @@ def main():
     dw = upload(w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush_sink = torch.empty(1, dtype=torch.int64, device="cuda")
+
+    def flush_l2():
+        # write a buffer larger than L2, then read it back: the KV lines are gone
+        # and no dirty lines are left to be written back during the timed step
+        flush.fill_(1)
+        torch.sum(flush.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
 
     def step_split(ev):
         ev[0].record(stream)
@@ -295,7 +303,7 @@ def main():
         ev[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step_split([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     if memra.read_status(dw.cache):
@@ -309,7 +317,7 @@ def main():
     sampler.start()
     time.sleep(0.3)
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step_split(evs[i])
     torch.cuda.synchronize()
     if world > 1:
@@ -354,12 +362,12 @@ def main():
         out_host.copy_(dw.out, non_blocking=True)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
