@@ -108,7 +108,7 @@ def test_query_shapes(q_len, n_heads, n_kv_heads, D):
     assert_out_close(w, res, attention.reference(w))
 
 
-@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 1023, 1024, 1025, 2048, 2049])
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 511, 512, 513, 1023, 1024, 1025, 2049])
 def test_context_edges(T):
     w = W.make_workload(f"edge{T}", batch=1, q_len=1, n_heads=8, n_kv_heads=1, head_dim=128, k_fmt="q8_0",
                         v_fmt="q5_1", seed=T, seq_lens=[T], permute_pages=True, extra_pages=2)
