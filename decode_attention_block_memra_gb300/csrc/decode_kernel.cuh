@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
                 mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
-                const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk0[bb / 2] >> (16 * (bb & 1)))));
-                const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dk1[bb / 2] >> (16 * (bb & 1)))));
+                const float2 dd0 = __half22float2(*reinterpret_cast<const __half2 *>(&dk0[bb / 2]));
+                const float2 dd1 = __half22float2(*reinterpret_cast<const __half2 *>(&dk1[bb / 2]));
+                const float d0 = (bb & 1) ? dd0.y : dd0.x, d1 = (bb & 1) ? dd1.y : dd1.x;
                 sc[n][0] = fmaf(d0, acc[0], sc[n][0]);
                 sc[n][1] = fmaf(d0, acc[1], sc[n][1]);
                 sc[n][2] = fmaf(d1, acc[2], sc[n][2]);
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                   // it at 16 (pairs 0, 2) or 256 (pairs 1, 3) of the fp16 value.
                   const int k = 2 * bh + h;
                   const uint32_t x0 = hw[bp] << (4 - k);
-                  const uint32_t x1 = hw[bp] >> (4 + k);
+                  const uint32_t x1 = (hw[bp] >> 8) << (4 - k);          // (H >> 8) << (4 - k) == H >> (4 + k) on the bits kept
                   a[0] |= x0 & 0x00100010u;
                   a[1] |= x0 & 0x01000100u;
                   a[2] |= x1 & 0x00100010u;
