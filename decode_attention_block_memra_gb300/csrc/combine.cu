@@ -4,7 +4,7 @@
 // kernel left (o_s = O_s / l_s, lse_s = m_s + log2 l_s) per split.  The exact
 // merge is  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max lse_s
 // (splits with no visible key have lse = -inf and weight 0).  One CTA per
-// row with up to 16 warps; warp w takes splits w, w+16, ... (four in flight),
+// row with up to 16 warps; warp w takes splits w, w+16, ... (eight in flight),
 // each lane owning D/32 consecutive outputs, so every split's partial is one
 // coalesced 512 B (D 128) or 1 KiB (D 256) read; the warps then reduce
 // through shared memory.  Launched as a programmatic dependent of the split
@@ -20,6 +20,7 @@ constexpr int kCombineMaxWarps = 16;
 template <int D>
 __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const CombineParams p) {
   constexpr int PER = D / 32;                       // outputs per lane
+  constexpr int BATCH = 8;                          // splits in flight per warp
   __shared__ float red[kCombineMaxWarps][D];
   __shared__ float redl[kCombineMaxWarps];
   __shared__ float mx[kCombineMaxWarps];
@@ -38,56 +39,55 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
     return;
   }
   const float *lse = p.lse_part + static_cast<size_t>(row) * p.nsplit_max;
-  float M = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += blockDim.x) M = fmaxf(M, lse[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) mx[warp] = M;
-  __syncthreads();
-  M = mx[0];
-  for (int w = 1; w < nw; ++w) M = fmaxf(M, mx[w]);
+  const float *op = p.o_part + static_cast<size_t>(row) * p.nsplit_max * D + lane * PER;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
-  if (M != -INFINITY) {
-    const float *op = p.o_part + static_cast<size_t>(row) * p.nsplit_max * D + lane * PER;
-    int s = warp;
-    // four splits in flight per warp
-    for (; s + 3 * nw < ns; s += 4 * nw) {
-      float4 x[4][PER / 4];
-      float wgt[4];
+  // Warp w owns splits w, w + nw, ...; each batch issues all of its loads
+  // (partials and their lse) before the block-wide maximum is known, so the
+  // whole row costs one memory round trip per BATCH x nw splits.
+  float M = -INFINITY;
+  for (int base = 0; base < ns; base += BATCH * nw) {
+    float4 x[BATCH][PER / 4];
+    float ls[BATCH];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 *src = reinterpret_cast<const float4 *>(op + static_cast<size_t>(s + u * nw) * D);
+    for (int u = 0; u < BATCH; ++u) {
+      const int sidx = base + warp + u * nw;
+      const bool ok = sidx < ns;
+      ls[u] = ok ? lse[sidx] : -INFINITY;
+      const float4 *src = reinterpret_cast<const float4 *>(op + static_cast<size_t>(ok ? sidx : 0) * D);
 #pragma unroll
-        for (int q4 = 0; q4 < PER / 4; ++q4) x[u][q4] = src[q4];
-        wgt[u] = fast_exp2(lse[s + u * nw] - M);
-      }
+      for (int q4 = 0; q4 < PER / 4; ++q4) x[u][q4] = ok ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // block-wide maximum of this batch's lse (and the previous batches')
+    float m = M;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        L += wgt[u];
+    for (int u = 0; u < BATCH; ++u) m = fmaxf(m, ls[u]);
+    if (lane == 0) mx[warp] = m;
+    __syncthreads();
+    float mnew = mx[0];
+    for (int w = 1; w < nw; ++w) mnew = fmaxf(mnew, mx[w]);
+    __syncthreads();
+    if (mnew != -INFINITY) {
+      // rescale what was accumulated against the old maximum
+      const float alpha = M == -INFINITY ? 0.f : fast_exp2(M - mnew);
+      L *= alpha;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] *= alpha;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const float wgt = ls[u] == -INFINITY ? 0.f : fast_exp2(ls[u] - mnew);
+        L += wgt;
 #pragma unroll
         for (int q4 = 0; q4 < PER / 4; ++q4) {
-          acc[4 * q4 + 0] = fmaf(wgt[u], x[u][q4].x, acc[4 * q4 + 0]);
-          acc[4 * q4 + 1] = fmaf(wgt[u], x[u][q4].y, acc[4 * q4 + 1]);
-          acc[4 * q4 + 2] = fmaf(wgt[u], x[u][q4].z, acc[4 * q4 + 2]);
-          acc[4 * q4 + 3] = fmaf(wgt[u], x[u][q4].w, acc[4 * q4 + 3]);
+          acc[4 * q4 + 0] = fmaf(wgt, x[u][q4].x, acc[4 * q4 + 0]);
+          acc[4 * q4 + 1] = fmaf(wgt, x[u][q4].y, acc[4 * q4 + 1]);
+          acc[4 * q4 + 2] = fmaf(wgt, x[u][q4].z, acc[4 * q4 + 2]);
+          acc[4 * q4 + 3] = fmaf(wgt, x[u][q4].w, acc[4 * q4 + 3]);
         }
       }
-    }
-    for (; s < ns; s += nw) {
-      const float wgt = fast_exp2(lse[s] - M);
-      const float4 *src = reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D);
-      L += wgt;
-#pragma unroll
-      for (int q4 = 0; q4 < PER / 4; ++q4) {
-        const float4 x = src[q4];
-        acc[4 * q4 + 0] = fmaf(wgt, x.x, acc[4 * q4 + 0]);
-        acc[4 * q4 + 1] = fmaf(wgt, x.y, acc[4 * q4 + 1]);
-        acc[4 * q4 + 2] = fmaf(wgt, x.z, acc[4 * q4 + 2]);
-        acc[4 * q4 + 3] = fmaf(wgt, x.w, acc[4 * q4 + 3]);
-      }
+      M = mnew;
     }
   }
 #pragma unroll

@@ -99,7 +99,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   const bool live = row < p.n_tok * p.n_kv_heads;
   const int tok = live ? row / p.n_kv_heads : 0;
   const int head = live ? row % p.n_kv_heads : 0;
-  int slot = live ? p.slots[tok] : -1;
+  // The slot and the row's K/V are loaded together (one memory round trip).
+  int slot = -1;
+  uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+  if (live) {
+    const size_t off = (static_cast<size_t>(tok) * p.n_kv_heads + head) * D + 8 * l;
+    slot = p.slots[tok];
+    rk = *reinterpret_cast<const uint4 *>(p.k + off);
+    rv = *reinterpret_cast<const uint4 *>(p.v + off);
+  }
   if (slot >= p.num_pages * kPage) {
     if (l == 0) flag_error(p.status, MEMRA_DEVERR_BAD_SLOT);
     slot = -1;
@@ -114,11 +122,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   // carry zeros), stores only on active rows.
   float xk[8], xv[8];
   {
-    uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
-    if (act) {
-      const size_t off = (static_cast<size_t>(tok) * p.n_kv_heads + head) * D + 8 * l;
-      rk = *reinterpret_cast<const uint4 *>(p.k + off);
-      rv = *reinterpret_cast<const uint4 *>(p.v + off);
+    if (!act) {
+      rk = make_uint4(0, 0, 0, 0);
+      rv = make_uint4(0, 0, 0, 0);
     }
     const __half2 *hk = reinterpret_cast<const __half2 *>(&rk);
     const __half2 *hv = reinterpret_cast<const __half2 *>(&rv);
