@@ -88,7 +88,8 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   // else 2), in steps of 4 so that page i and page i + depth meet the same warp.
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
   const int ctas_per_sm = (D == 128 && nt == 1) ? 4 : 2;
-  const size_t budget = (226 * 1024) / ctas_per_sm - 2048;
+  const size_t qbytes = static_cast<size_t>(kWarps) * nt * (D / 32) * 512;     // warp-private Q fragments
+  const size_t budget = (226 * 1024) / ctas_per_sm - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
   int ns = static_cast<int>(budget / stage) & ~3;
   if (ns > 32) ns = 32;
   if (ns < 4) ns = 4;
@@ -101,7 +102,7 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   pl->nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
   pl->num_stages = ns;
   pl->ctas_per_sm = ctas_per_sm;
-  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(kSplitPagesMax);
+  pl->smem = region + 16 * static_cast<size_t>(ns) + 4 * static_cast<size_t>(kSplitPagesMax) + qbytes;
   return MEMRA_OK;
 }
 

@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
 
   const int g = lane >> 2, c = lane & 3;
   const int row_base = gr * ROWS_W;
+  // Q^T fragments live in shared memory (warp-private, fragment order: one
+  // conflict-free 16-byte load per block and n-tile), not in 16+ registers.
+  const uint32_t qsm = smem_addr(smem + region + 16 * NS + 4 * kSplitPagesMax) + warp * (NT * NB * 512);
 
   // Q^T fragments (B operand of S^T = K^ Q^T): row 8n+g, dims 32bb+8c..+7.
   uint4 qf[NT][NB];
@@ -261,6 +264,17 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
       corrb[n][1] = bw[1];
     }
   }
+
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+      const uint4 v = qf[n][bb];
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qsm + ((n * NB + bb) * 32 + lane) * 16), "r"(v.x),
+                   "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    }
+  }
+  __syncwarp();
 
   float o[NT][2 * NB][4];
   float mt[NT][4];
@@ -331,10 +345,11 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
             k_pairs<KF>(t1hi, a1[1], a1[3]);
 #pragma unroll
               for (int n = 0; n < NT; ++n) {
+                const uint4 qv = lds128(qsm + ((n * NB + bb) * 32 + lane) * 16);
               if constexpr (kK8) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_16816(acc, a0, qf[n][bb].x, qf[n][bb].y);
-                mma_16816(acc, a1, qf[n][bb].z, qf[n][bb].w);
+                mma_16816(acc, a0, qv.x, qv.y);
+                mma_16816(acc, a1, qv.z, qv.w);
                 const float2 dd0 = __half22float2(*reinterpret_cast<const __half2 *>(&dk0[bb / 2]));
                 const float2 dd1 = __half22float2(*reinterpret_cast<const __half2 *>(&dk1[bb / 2]));
                 const float d0 = (bb & 1) ? dd0.y : dd0.x, d1 = (bb & 1) ? dd1.y : dd1.x;
@@ -343,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                 sc[n][2] = fmaf(d1, acc[2], sc[n][2]);
                 sc[n][3] = fmaf(d1, acc[3], sc[n][3]);
               } else {
-                mma_16816(sc[n], a0, qf[n][bb].x, qf[n][bb].y);
-                mma_16816(sc[n], a1, qf[n][bb].z, qf[n][bb].w);
+                mma_16816(sc[n], a0, qv.x, qv.y);
+                mma_16816(sc[n], a1, qv.z, qv.w);
               }
             }
           }
