@@ -8,11 +8,12 @@
 // plain decode and MTP verify are the memra README's "Speculative decoding"
 // item; the 262,144-token contexts its "Long context and larger models" item.
 //
-// How (one CTA = 4 consumer warps + 1 producer warp):
-//  * The producer warp reads the split's page ids and streams each page's K
-//    and V segments (one contiguous bulk copy each, 16-byte aligned, evict-
-//    first in L2) into a ring of shared-memory stages guarded by mbarriers.
-//  * Consumer warp w takes every R-th page (R = 4 / row groups).  Per page:
+// How (one CTA = 4 warps):
+//  * Warp w takes every R-th page of the split (R = 4 / row groups) and owns
+//    the ring stages of those pages.  The page lane's first warp streams each
+//    page's K and V segments (one contiguous bulk copy each, 16-byte aligned,
+//    evict-first in L2) into its stages, `num_stages` pages ahead, completing
+//    on per-stage mbarriers, and refills a stage as soon as it is read.  Per page:
 //    S^T[16 tokens x 8 rows] = K^ Q^T on the tensor cores (m16n8k16, fp16 in,
 //    fp32 out) with the K codes converted to fp16 in registers; the q8_0 block
 //    scale multiplies each 32-element block's partial sum, so K^ is exact.
@@ -21,6 +22,11 @@
 //    operand, then O^T[D x rows] += V^T P^T with the V codes converted in
 //    registers and the per-token block scale folded into P; q5_1's +m term is
 //    one extra MMA (blocks x tokens) * P^T.
+//  * q8_0 K codes are stored biased (q + 128) and become fp16 1152 + q with
+//    one byte permute per pair; one more MMA per page, with the block scales
+//    as A and -1152 * sum(Q) as B (fp16 hi + lo), takes the bias out.
+//  * The reference maximum of a row moves only when a score passes it by more
+//    than 2 (log2 units), so O and l are rescaled only then.
 //  * At the end the consumer warps merge their (m, l, O) through shared
 //    memory; a split that covers the whole sequence writes fp16 output,
 //    otherwise an fp32 partial for the combine kernel.
@@ -118,13 +124,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
   constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
   constexpr bool kVq = kQ5 || kQ4;
   constexpr bool kK8 = KF == MEMRA_KV_Q8_0;
-  // V codes enter the MMA with their fp16 offset (1024 + code, 1024 + 16 code);
-  // one extra MMA per block with an all-ones A sums the block's B operand, and
-  // the epilogue subtracts offset x sum (and divides slot g+8 by 16).  Used
-  // where the extra accumulators fit (8 query rows per warp).
-  constexpr bool kOnesMma = kVq && NT == 1;
   constexpr float kLazy = 2.f;
-  const uint32_t kOnesA[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
 
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -278,17 +278,12 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
 
   float o[NT][2 * NB][4];
   float mt[NT][4];
-  float ones[kOnesMma ? NT : 1][kOnesMma ? NB : 1][4];
   float mrow[NT][2], lrow[NT][2];
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
 #pragma unroll
     for (int i = 0; i < 2 * NB; ++i) o[n][i][0] = o[n][i][1] = o[n][i][2] = o[n][i][3] = 0.f;
     mt[n][0] = mt[n][1] = mt[n][2] = mt[n][3] = 0.f;
-    if constexpr (kOnesMma) {
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) ones[n][bb][0] = ones[n][bb][1] = ones[n][bb][2] = ones[n][bb][3] = 0.f;
-    }
     mrow[n][0] = mrow[n][1] = -INFINITY;
     lrow[n][0] = lrow[n][1] = 0.f;
   }
@@ -429,13 +424,6 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                 o[n][i2][2 + u] *= alpha;
               }
               if constexpr (kQ5) mt[n][u] *= alpha;
-              if constexpr (kOnesMma) {
-#pragma unroll
-                  for (int bb = 0; bb < NB; ++bb) {
-                  ones[n][bb][u] *= alpha;
-                  ones[n][bb][2 + u] *= alpha;
-                }
-              }
             }
           }
         }
@@ -499,7 +487,6 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                 for (int n = 0; n < NT; ++n) {
                 bs[n][0] = hmul2_u32(pb[n][0], dv[bb].x);
                 bs[n][1] = hmul2_u32(pb[n][1], dv[bb].y);
-                if constexpr (kOnesMma) mma_16816(ones[n][bb], kOnesA, bs[n][0], bs[n][1]);
               }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -525,14 +512,14 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
                   a[2] |= x1 & 0x00100010u;
                   a[3] |= x1 & 0x01000100u;
                 }
-                if constexpr (!kOnesMma) {
-                  constexpr uint32_t kSub0 = kQ5 ? 0x64006400u : 0x64086408u;      // 1024 | 1032
-                  constexpr uint32_t kSub1 = kQ5 ? 0xD400D400u : 0xD480D480u;      // -64 | -72
-                  a[0] = hsub2_u32(a[0], kSub0);
-                  a[2] = hsub2_u32(a[2], kSub0);
-                  a[1] = hfma2_u32(a[1], 0x2C002C00u, kSub1);                      // x / 16 + (-64 | -72)
-                  a[3] = hfma2_u32(a[3], 0x2C002C00u, kSub1);
-                }
+                // exact back to the code: x - 1024 (q4_0: - 1032), x / 16 - 64 (q4_0: - 72),
+                // on the FMA pipe (the ALU pipe is the busier one)
+                constexpr uint32_t kSub0 = kQ5 ? 0x64006400u : 0x64086408u;      // 1024 | 1032
+                constexpr uint32_t kSub1 = kQ5 ? 0xD400D400u : 0xD480D480u;      // -64 | -72
+                a[0] = hsub2_u32(a[0], kSub0);
+                a[2] = hsub2_u32(a[2], kSub0);
+                a[1] = hfma2_u32(a[1], 0x2C002C00u, kSub1);
+                a[3] = hfma2_u32(a[3], 0x2C002C00u, kSub1);
 #pragma unroll
                   for (int n = 0; n < NT; ++n) mma_16816(o[n][2 * bb + h], a, bs[n][0], bs[n][1]);
               }
@@ -613,25 +600,6 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       lrow[n][u] = l;
-    }
-  }
-  if constexpr (kOnesMma) {
-    // remove the fp16 code offsets: slot g holds sum B (1024 + code) (+8 for
-    // q4_0's stored code), slot g+8 sum B (1024 + 16 stored code)
-    constexpr float kOff0 = kQ5 ? 1024.f : 1032.f, kOff1 = kQ5 ? 1024.f : 1152.f;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float *v = o[n][2 * bb + h];
-          v[0] = fmaf(-kOff0, ones[n][bb][0], v[0]);
-          v[1] = fmaf(-kOff0, ones[n][bb][1], v[1]);
-          v[2] = fmaf(-kOff1, ones[n][bb][0], v[2]) * 0.0625f;
-          v[3] = fmaf(-kOff1, ones[n][bb][1], v[3]) * 0.0625f;
-        }
-      }
     }
   }
   __syncthreads();                       // every warp is done with the ring
