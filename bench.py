@@ -138,6 +138,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(seconds: float, world: int, device=None) -> float:
+    """The job's time: the slowest rank's (replicas run independently; no data exchange)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank processes its own replica of the workload."""
+    return world * tokens_per_step * steps / seconds
+
+
 def cpu_baseline(workload: str, reps: int) -> dict:
     """The oracle, as it stands, timed on host cores in a single-threaded subprocess."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
@@ -343,13 +359,9 @@ def main():
         split_pass(*e)
     torch.cuda.synchronize()
     k2_ms = [a.elapsed_time(b) for a, b in kev]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, "cuda")
     tokens_per_step = w.batch * w.q_len
-    value = world * tokens_per_step * args.steps / total_s
+    value = job_throughput(tokens_per_step, args.steps, world, total_s)
     kv_bytes = unique_kv_bytes(w)
     peak, peak_kind = measured_peaks()
     k2_avg_s = statistics.mean(k2_ms) / 1e3
@@ -391,12 +403,8 @@ def main():
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_total = sum(e2e_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * tokens_per_step * args.steps / e2e_total
+    e2e_total = max_over_ranks(sum(e2e_ms) / 1e3, world, "cuda")
+    e2e_value = job_throughput(tokens_per_step, args.steps, world, e2e_total)
 
     if rank == 0:
         traffic = stored_traffic(w.name)
