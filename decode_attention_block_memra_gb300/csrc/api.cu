@@ -60,9 +60,11 @@ int split_target(const Plan &pl, int n_kv_heads) {
   return t > 0 ? t : 1;
 }
 
+int warps_for(int D, int nt) { return (D == 128 && nt == 1) ? kWarpsFor<128, 1> : kWarpsFor<256, 1>; }
+
 size_t merge_bytes(int D, int nt) {
   const size_t rows_w = 8 * nt, nb = D / 32;
-  const size_t w = kWarps;
+  const size_t w = warps_for(D, nt);
   return (w * rows_w * D + 2 * w * rows_w + w * rows_w * nb) * 4;
 }
 
@@ -82,17 +84,18 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
     ngrp = static_cast<int>(ceil_div(qg, 8));
   }
   if (ngrp == 3) ngrp = 4;
-  if (ngrp > kWarps) return MEMRA_ERR_UNSUPPORTED;
-  // Pipeline depth: as many 16-token pages in flight as fit beside the CTAs
-  // that share an SM (4 CTAs of 4 warps at head_dim 128 with 8 rows per warp,
-  // else 2), in steps of 4 so that page i and page i + depth meet the same warp.
+  const int W = warps_for(D, nt);
+  if (ngrp > W) return MEMRA_ERR_UNSUPPORTED;
+  // Pipeline depth: as many 16-token pages in flight as fit beside the other
+  // CTA of the SM, in steps of the warp count so that page i and page
+  // i + depth meet the same warp.
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
-  const int ctas_per_sm = (D == 128 && nt == 1) ? 4 : 2;
-  const size_t qbytes = static_cast<size_t>(kWarps) * nt * (D / 32) * 512;     // warp-private Q fragments
+  const int ctas_per_sm = 2;
+  const size_t qbytes = static_cast<size_t>(W) * nt * (D / 32) * 512;     // warp-private Q fragments
   const size_t budget = (226 * 1024) / ctas_per_sm - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
-  int ns = static_cast<int>(budget / stage) & ~3;
+  int ns = static_cast<int>(budget / stage) & ~(W - 1);
   if (ns > 32) ns = 32;
-  if (ns < 4) ns = 4;
+  if (ns < W) ns = W;
   size_t region = stage * ns;
   const size_t mb = merge_bytes(D, nt);
   if (mb > region) region = mb;

@@ -71,16 +71,20 @@ cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
 cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
                              cudaStream_t stream);
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
+// Warps per CTA: 8 at head_dim 128 with 8 query rows per warp (fewer pages
+// per warp for short sequences; 2 CTAs/SM still give 16 warps), else 4.
+template <int D, int NT>
+constexpr int kWarpsFor = (D == 128 && NT == 1) ? 8 : 4;
+constexpr int kMaxWarps = 8;
 
 template <int D, int NT>
 struct MergeLayout {
+  static constexpr int kW = kWarpsFor<D, NT>;
   static constexpr int kRowsW = 8 * NT;
   static constexpr int kNb = D / 32;
-  static constexpr int kO = kWarps * kRowsW * D;          // floats
-  static constexpr int kM = kWarps * kRowsW;
-  static constexpr int kTerm = kWarps * kRowsW * kNb;
+  static constexpr int kO = kW * kRowsW * D;          // floats
+  static constexpr int kM = kW * kRowsW;
+  static constexpr int kTerm = kW * kRowsW * kNb;
   static constexpr int kBytes = (kO + 2 * kM + kTerm) * 4;
 };
 
@@ -112,13 +116,15 @@ __device__ __forceinline__ uint32_t shift_const(uint32_t x) {
 }
 
 template <int D, int KF, int VF, int NT>
-__global__ void __launch_bounds__(kThreads, (NT == 1 && D == 128 ? 4 : (D == 128 ? 2 : 2)))
+__global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
     decode_split_kernel(const DecodeParams p) {
   constexpr int NB = D / 32;
   constexpr int KSEG = k_seg_bytes(KF, D);
   constexpr int VSEG = v_seg_bytes(VF, D);
   constexpr int STAGE = KSEG + VSEG;
   using ML = MergeLayout<D, NT>;
+  constexpr int kWarps = kWarpsFor<D, NT>;
+  constexpr int kThreads = kWarps * 32;
   constexpr int ROWS_W = ML::kRowsW;
   constexpr bool kQ5 = VF == MEMRA_KV_Q5_1;
   constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
@@ -690,7 +696,7 @@ cudaError_t launch_one(const DecodeParams &p, dim3 grid, size_t smem, cudaStream
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(decode_split_kernel<D, KF, VF, NT>, grid, dim3(kThreads), smem, st, p);
+  return launch_pdl(decode_split_kernel<D, KF, VF, NT>, grid, dim3(kWarpsFor<D, NT> * 32), smem, st, p);
 }
 
 template <int D, int NT>
