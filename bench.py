@@ -264,6 +264,8 @@ def main():
     ap.add_argument("--formats", default=None, help="K/V formats overriding the workload's, e.g. q8_0/q4_0")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-call", action="store_true",
+                    help="time memra_kv_append + memra_decode_attn instead of the fused memra_decode_step")
     ap.add_argument("--cpu-reps", type=int, default=5)
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -307,13 +309,28 @@ def main():
         flush.fill_(1)
         torch.sum(flush.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
 
+    B, Q = w.batch, w.q_len
+    k_new = dw.step_k.view(B, Q, w.n_kv_heads, w.head_dim)
+    v_new = dw.step_v.view(B, Q, w.n_kv_heads, w.head_dim)
+
+    def hot_path():
+        # store the step's rows and attend: one memra_decode_step (split-K with
+        # the rows stored inside, then the combine), or the two-call form
+        if args.two_call:
+            memra.kv_append(dw.cache, dw.step_k, dw.step_v, dw.step_slots, stream=stream)
+            memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
+                              w.sm_scale, stream=stream)
+        else:
+            memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out,
+                              dw.workspace, w.sm_scale, stream=stream)
+
+    launches_per_step = 3 if args.two_call else 2
+
     def step(ev0, ev1):
         # one pass of the hot path through the public entry points, events only
-        # at its two ends so the three launches chain as they do in use
+        # at its two ends so the launches chain as they do in use
         ev0.record(stream)
-        memra.kv_append(dw.cache, dw.step_k, dw.step_v, dw.step_slots, stream=stream)
-        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
-                          w.sm_scale, stream=stream)
+        hot_path()
         ev1.record(stream)
 
     def split_pass(ev0, ev1):
@@ -371,9 +388,11 @@ def main():
     host = {
         "q": torch.from_numpy(w.q).pin_memory(),
         "k": dw.step_k.cpu().pin_memory(), "v": dw.step_v.cpu().pin_memory(),
-        "slots": dw.step_slots.cpu().pin_memory(), "seq_lens": dw.seq_lens.cpu().pin_memory(),
+        "seq_lens": dw.seq_lens.cpu().pin_memory(),
         "page_table": dw.page_table.cpu().pin_memory(),
     }
+    if args.two_call:
+        host["slots"] = dw.step_slots.cpu().pin_memory()      # the fused step finds slots in the page table
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -382,12 +401,11 @@ def main():
         dw.q.copy_(host["q"], non_blocking=True)
         dw.step_k.copy_(host["k"], non_blocking=True)
         dw.step_v.copy_(host["v"], non_blocking=True)
-        dw.step_slots.copy_(host["slots"], non_blocking=True)
+        if args.two_call:
+            dw.step_slots.copy_(host["slots"], non_blocking=True)
         dw.seq_lens.copy_(host["seq_lens"], non_blocking=True)
         dw.page_table.copy_(host["page_table"], non_blocking=True)
-        memra.kv_append(dw.cache, dw.step_k, dw.step_v, dw.step_slots, stream=stream)
-        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
-                          w.sm_scale, stream=stream)
+        hot_path()
         out_host.copy_(dw.out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -426,7 +444,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_total / args.steps * 1e3},
-            "gpu_launches": 3 * args.steps,      # append, split-K, combine per timed step
+            # per timed step: split-K (rows stored inside) + combine, or append + split-K + combine
+            "gpu_launches": launches_per_step * args.steps,
+            "step_form": "two-call (memra_kv_append + memra_decode_attn)" if args.two_call
+            else "fused (memra_decode_step)",
             "clocks": clocks,
             "device_flags": flags,
         }

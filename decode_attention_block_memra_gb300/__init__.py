@@ -69,6 +69,10 @@ _SIGS = {
     "memra_decode_attn_combine": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p] +
                                   [ctypes.c_int32] * 6 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                           ctypes.c_void_p]),
+    "memra_decode_step": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
+                          [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                                  ctypes.c_void_p]),
     "memra_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
                                                  ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
                                   [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
@@ -204,6 +208,17 @@ def decode_attn_combine(cache: KVCache, seq_lens, max_seq_len: int, max_pages_pe
     _check(lib().memra_decode_attn_combine(cache.ref, _ptr(seq_lens), int(max_seq_len), int(max_pages_per_seq), batch,
                                            q_len, n_heads, cache.head_dim, _ptr(workspace), ws_bytes, _ptr(out),
                                            _stream(stream)), "memra_decode_attn_combine")
+
+
+def decode_step(cache: KVCache, k_new, v_new, q, page_table, seq_lens, max_seq_len: int, out, workspace,
+                sm_scale=None, stream=None) -> None:
+    """memra_decode_step: store the step's rows (k_new, v_new fp16 [B, Q, Hkv, D]) and attend, in one pass.
+
+    seq_lens include the Q new tokens; their rows go to the positions
+    seq_lens[b] - Q .. seq_lens[b] - 1 of each sequence's pages.
+    """
+    a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
+    _check(lib().memra_decode_step(a[0], _ptr(k_new), _ptr(v_new), *a[1:], _stream(stream)), "memra_decode_step")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

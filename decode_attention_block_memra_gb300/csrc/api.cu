@@ -152,7 +152,8 @@ int check_decode(const DecodeArgs &a) {
   return MEMRA_OK;
 }
 
-int run_partials(const DecodeArgs &a, cudaStream_t st) {
+// k_new / v_new: the fused append's rows, or null for attention alone.
+int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cudaStream_t st) {
   const memra_kv_cache &c = *a.cache;
   Plan pl;
   const int group = a.n_heads / a.n_kv_heads;
@@ -171,6 +172,8 @@ int run_partials(const DecodeArgs &a, cudaStream_t st) {
   p.o_part = static_cast<float *>(a.workspace);
   p.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + lse_off);
   p.status = c.status;
+  p.k_new = static_cast<const __half *>(k_new);
+  p.v_new = static_cast<const __half *>(v_new);
   p.n_kv_heads = c.n_kv_heads;
   p.num_pages = c.num_pages;
   p.max_pages = a.max_pages_per_seq;
@@ -186,6 +189,7 @@ int run_partials(const DecodeArgs &a, cudaStream_t st) {
   const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
+  p.k_scale = c.k_scale;
   // no sequence has more splits than min(ceil(T/1024), max(target, ceil(T/8192)))
   const int64_t most = std::min<int64_t>(pl.nsplit_max, std::max<int64_t>(p.split_target,
                                                                           ceil_div(a.max_seq_len, kSplitTokensMax)));
@@ -266,7 +270,7 @@ int memra_decode_attn_partials(const memra_kv_cache *cache, const void *q, const
                n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
   int st = check_decode(a);
   if (st || batch == 0) return st;
-  return run_partials(a, static_cast<cudaStream_t>(stream));
+  return run_partials(a, nullptr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_lens, int32_t max_seq_len,
@@ -296,7 +300,25 @@ int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t 
   int st = check_decode(a);
   if (st || batch == 0) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_partials(a, s);
+  st = run_partials(a, nullptr, nullptr, s);
+  if (st) return st;
+  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
+                     out, s);
+}
+
+int memra_decode_step(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                      const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                      int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                      int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+                      void *stream) {
+  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
+  int st = check_decode(a);
+  if (st || batch == 0) return st;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return MEMRA_ERR_INVALID_ARG;
+  if (max_seq_len < q_len) return MEMRA_ERR_INVALID_ARG;     // no sequence can hold the new rows
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_partials(a, k_new, v_new, s);
   if (st) return st;
   return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
                      out, s);

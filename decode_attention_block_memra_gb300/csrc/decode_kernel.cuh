@@ -39,7 +39,7 @@
 
 #include <type_traits>
 
-#include "memra_device.cuh"
+#include "kv_quant.cuh"
 
 namespace memra {
 
@@ -53,9 +53,14 @@ struct DecodeParams {
   float *o_part;      // [rows][nsplit_max][D]
   float *lse_part;    // [rows][nsplit_max]
   int32_t *status;
+  // Fused append (null when the step's rows are already in the pools): the
+  // K and V rows of the q_len new tokens, fp16 [batch][q_len][n_kv_heads][D],
+  // stored at positions seq_len - q_len .. seq_len - 1 before they are read.
+  const __half *k_new;
+  const __half *v_new;
   int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group, qg;
   int nsplit_max, num_stages, ngrp, split_target;
-  float scale_log2, v_scale;
+  float scale_log2, v_scale, k_scale;
 };
 
 struct CombineParams {
@@ -193,8 +198,15 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
       mbar_arrive(bar);
     }
   };
+  // New tokens of this step that fall in this split (fused append only): their
+  // pages [app_lo, app_hi] are copied in only after the rows are stored.
+  const int app_pos0 = max(max(T - p.q_len, tok0), 0);
+  const int app_n = p.k_new ? max(min(T, tok0 + C) - app_pos0, 0) : 0;
+  const int app_lo = app_n ? app_pos0 / kPage - tok0 / kPage : npages;
+  const int app_hi = app_n ? (app_pos0 + app_n - 1) / kPage - tok0 / kPage : -1;
   if (issuer && lane == 0) {
-    for (int i = r; i < min(NS, npages); i += R) issue(i, i);
+    for (int i = r; i < min(NS, npages); i += R)
+      if (i < app_lo || i > app_hi) issue(i, i);
   }
 
   const int g = lane >> 2, c = lane & 3;
@@ -281,6 +293,37 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
     }
   }
   __syncwarp();
+
+  if (app_n > 0) {
+    // Fused append: quantize this KV head's rows of the new tokens into their
+    // pool pages (one row per D/8 lanes, the same code as the append kernel),
+    // then order those generic stores before the bulk copies that read them.
+    constexpr int kLanesRow = D / 8;
+    constexpr int kRowsPass = kThreads / kLanesRow;
+    const QuantTarget dst{const_cast<uint8_t *>(p.k_pool), const_cast<uint8_t *>(p.v_pool), p.n_kv_heads, KF, VF,
+                          p.k_scale, p.v_scale};
+    const int l = tid % kLanesRow;
+    const int first_new = T - p.q_len;       // position of new token 0
+    for (int j0 = 0; j0 < app_n; j0 += kRowsPass) {
+      const int j = j0 + tid / kLanesRow;
+      const int pos = app_pos0 + j;
+      int page = -1;
+      uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+      if (j < app_n) {
+        page = pid_s[pos / kPage - tok0 / kPage];
+        const size_t off = ((static_cast<size_t>(b) * p.q_len + (pos - first_new)) * p.n_kv_heads + kvh) * D + 8 * l;
+        rk = *reinterpret_cast<const uint4 *>(p.k_new + off);
+        rv = *reinterpret_cast<const uint4 *>(p.v_new + off);
+      }
+      quantize_store_row<D>(dst, page >= 0, max(page, 0), pos % kPage, kvh, l, rk, rv);
+    }
+    fence_proxy_async_global();
+    __syncthreads();
+    if (issuer && lane == 0) {
+      for (int i = r; i < min(NS, npages); i += R)
+        if (i >= app_lo && i <= app_hi) issue(i, i);
+    }
+  }
 
   float o[NT][2 * NB][4];
   float mt[NT][4];

@@ -1,0 +1,224 @@
+// Quantize-and-store of one K/V row into the paged pools: the block rules
+// and byte layout stated in include/memra.h, shared by the append kernel and
+// by the decode kernel's fused append.  The rounding is exact in float32 (see
+// kv_append.cu).
+#pragma once
+
+#include "memra_device.cuh"
+
+namespace memra {
+
+struct QuantTarget {
+  uint8_t *k_pool;
+  uint8_t *v_pool;
+  int n_kv_heads, k_fmt, v_fmt;
+  float k_scale, v_scale;
+};
+
+__device__ __forceinline__ float group4_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float group4_min(float x) {
+  x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fminf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+
+__device__ __forceinline__ void store_half(uint8_t *p, __half h) {
+  *reinterpret_cast<__half *>(p) = h;
+}
+
+// a - b = hi + lo exactly (TwoSum of a and -b).
+__device__ __forceinline__ void two_diff(float a, float b, float &hi, float &lo) {
+  hi = __fsub_rn(a, b);
+  const float bb = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(-b, bb));
+}
+
+// fp16 round-to-nearest-even of (hi + lo) / k for hi + lo >= 0 and k in {7, 31, 127}.
+__device__ __forceinline__ __half fp16_quotient_rne(float hi, float lo, float k) {
+  unsigned short hb = __half_as_ushort(__float2half_rn(__fdiv_rn(hi, k)));
+  const float v = __half2float(__ushort_as_half(hb));
+  const float up_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb + 1))));
+  const float t_up = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, up_mid)), lo);     // sign of x/k - up_mid
+  if (t_up > 0.f || (t_up == 0.f && (hb & 1))) {
+    ++hb;
+  } else if (hb > 0) {
+    const float dn_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb - 1))));
+    const float t_dn = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, dn_mid)), lo);
+    if (t_dn < 0.f || (t_dn == 0.f && (hb & 1))) --hb;
+  }
+  return __ushort_as_half(hb);
+}
+
+// clamp(rne((hi + lo) / d), lo_q, hi_q) for the stored fp16 d (as float); 0 when d == 0.
+__device__ __forceinline__ int quant_code(float hi, float lo, float d, int lo_q, int hi_q) {
+  if (d == 0.f) return 0;
+  float q0 = rintf(__fdiv_rn(hi, d));
+  const float e = __fsub_rn(hi, __fmul_rn(q0, d));          // exact
+  const float hd = 0.5f * d;
+  const float up = __fadd_rn(__fsub_rn(e, hd), lo);          // sign of x/d - (q0 + 1/2)
+  const int odd = static_cast<int>(q0) & 1;
+  if (up > 0.f || (up == 0.f && odd)) {
+    q0 += 1.f;
+  } else {
+    const float dn = __fadd_rn(__fadd_rn(e, hd), lo);        // sign of x/d - (q0 - 1/2)
+    if (dn < 0.f || (dn == 0.f && odd)) q0 -= 1.f;
+  }
+  return min(max(static_cast<int>(q0), lo_q), hi_q);
+}
+
+// One (token, KV head) row per group of D/8 consecutive lanes; lane l of the
+// group holds elements 8l..8l+7 of the K row (rk) and of the V row (rv).
+// Every lane of the warp must call it (it shuffles within the group); only
+// rows with act set are stored, at token t of pool page `page`.
+template <int D>
+__device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool act, int page, int t, int head,
+                                                   int l, uint4 rk, uint4 rv) {
+  constexpr int kNb = D / 32;
+  const int b = l / 4;                            // block
+  const int cc = l % 4;                           // 8-element chunk within the block
+  // Both K and V of the row; shuffles below run on every lane (inactive rows
+  // carry zeros), stores only on active rows.
+  float xk[8], xv[8];
+  {
+    if (!act) {
+      rk = make_uint4(0, 0, 0, 0);
+      rv = make_uint4(0, 0, 0, 0);
+    }
+    const __half2 *hk = reinterpret_cast<const __half2 *>(&rk);
+    const __half2 *hv = reinterpret_cast<const __half2 *>(&rv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 a = __half22float2(hk[i]);
+      float2 c = __half22float2(hv[i]);
+      xk[2 * i] = a.x; xk[2 * i + 1] = a.y;
+      xv[2 * i] = c.x; xv[2 * i + 1] = c.y;
+    }
+  }
+
+  // ------------------------------------------------------------------ K ---
+  {
+    uint8_t *seg = dst.k_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * k_seg_bytes(dst.k_fmt, D);
+    const int tg = t % 8, tp = t / 8;
+    const int chunk = (tp * (kNb / 2) + b / 2) * 32 + 4 * tg + cc;
+    uint8_t code[8];
+    if (dst.k_fmt == MEMRA_KV_Q8_0) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xk[i]));
+      amax = group4_max(amax);
+      const __half dh = fp16_quotient_rne(amax, 0.f, 127.f);
+      const float d = __half2float(dh);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        code[i] = static_cast<uint8_t>(quant_code(xk[i], 0.f, d, -127, 127) + 128);   // stored biased
+      if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        code[i] = __nv_cvt_float_to_fp8(__fdiv_rn(xk[i], dst.k_scale), __NV_SATFINITE, __NV_E4M3);
+    }
+    if (act) {
+      uint2 w;
+      w.x = code[0] | (code[1] << 8) | (code[2] << 16) | (static_cast<uint32_t>(code[3]) << 24);
+      w.y = code[4] | (code[5] << 8) | (code[6] << 16) | (static_cast<uint32_t>(code[7]) << 24);
+      *reinterpret_cast<uint2 *>(seg + chunk * 16 + (b % 2) * 8) = w;
+    }
+  }
+
+  // ------------------------------------------------------------------ V ---
+  {
+    uint8_t *seg = dst.v_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * v_seg_bytes(dst.v_fmt, D);
+    const int c = (t % 8) / 2, f = t % 2, pp = t / 8, k = 2 * f + pp;
+    // element i of this lane: r = 8*cc + i -> vg = 2*cc + i/4, h = (i%4)/2, s = i%2
+    if (dst.v_fmt == MEMRA_KV_FP8_E4M3) {
+      if (act) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int vg = 2 * cc + i / 4, h = (i % 4) / 2, s = i % 2;
+          const uint8_t byte = __nv_cvt_float_to_fp8(__fdiv_rn(xv[i], dst.v_scale), __NV_SATFINITE, __NV_E4M3);
+          seg[(b * 32 + 4 * vg + c) * 16 + 8 * h + 2 * (2 * pp + s) + f] = byte;
+        }
+      }
+    } else {
+      int q[8];
+      __half dh, mh = __float2half(0.f);
+      if (dst.v_fmt == MEMRA_KV_Q5_1) {
+        float mn = xv[0], mx = xv[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) { mn = fminf(mn, xv[i]); mx = fmaxf(mx, xv[i]); }
+        mn = group4_min(mn);
+        mx = group4_max(mx);
+        float rh, rl;
+        two_diff(mx, mn, rh, rl);
+        dh = fp16_quotient_rne(rh, rl, 31.f);
+        mh = __float2half_rn(mn);                      // exact: mn is an fp16 value
+        const float d = __half2float(dh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float xh, xl;
+          two_diff(xv[i], mn, xh, xl);
+          q[i] = quant_code(xh, xl, d, 0, 31);
+        }
+      } else {  // q4_0, nibble = q + 8
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xv[i]));
+        amax = group4_max(amax);
+        dh = fp16_quotient_rne(amax, 0.f, 7.f);
+        const float d = __half2float(dh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], 0.f, d, -8, 7) + 8;
+      }
+      // low nibbles: one byte per (vg, h) holding s = 0 (low) and s = 1 (high)
+      if (act) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int vg = 2 * cc + u;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i0 = 4 * u + 2 * h;
+            const uint8_t byte = static_cast<uint8_t>((q[i0] & 15) | ((q[i0 + 1] & 15) << 4));
+            seg[((b / 2) * 32 + 4 * vg + c) * 16 + (b % 2) * 8 + 4 * h + k] = byte;
+          }
+        }
+      }
+      if (dst.v_fmt == MEMRA_KV_Q5_1) {
+        // bit 4 of each code: the byte of (vg, token) holds bit 4*s + 2*(b%2) + h,
+        // so the even block's lane merges its partner's bits (shifted by 2).
+        uint32_t hn[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          hn[u] = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = e / 2, s = e % 2;
+            hn[u] |= static_cast<uint32_t>((q[4 * u + e] >> 4) & 1) << (4 * s + h);
+          }
+        }
+        const uint32_t mine = hn[0] | (hn[1] << 8);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 4);   // lane of block b^1
+        if (act && (b % 2) == 0) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int vg = 2 * cc + u;
+            const uint32_t lo = (mine >> (8 * u)) & 0x33u, hi = (other >> (8 * u)) & 0x33u;
+            seg[8 * D + ((4 * vg + c) * (kNb / 2) + b / 2) * 4 + k] = static_cast<uint8_t>(lo | (hi << 2));
+          }
+        }
+      }
+      if (act && cc == 0) {
+        const int poff = ((c * kNb + b) * 4 + 2 * pp + f) * 2;
+        if (dst.v_fmt == MEMRA_KV_Q5_1) {
+          store_half(seg + 10 * D + poff, dh);
+          store_half(seg + 11 * D + poff, mh);
+        } else {
+          store_half(seg + 8 * D + poff, dh);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace memra

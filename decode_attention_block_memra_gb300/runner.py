@@ -11,7 +11,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import KVCache, decode_attn, decode_attn_workspace_bytes, kv_append, read_status
+from . import KVCache, decode_attn, decode_attn_workspace_bytes, decode_step, kv_append, read_status
 
 
 @dataclass
@@ -27,9 +27,19 @@ class DeviceWorkload:
     step_v: object
     step_slots: object
 
-    def step(self, stream=None) -> None:
-        """One pass of the hot path: append the step's rows, then attend."""
+    def step(self, stream=None, fused: bool = False) -> None:
+        """One pass of the hot path: append the step's rows, then attend.
+
+        fused: one memra_decode_step (the split kernel stores the rows) instead
+        of memra_kv_append followed by memra_decode_attn.
+        """
         w = self.w
+        if fused:
+            B, Q = w.batch, w.q_len
+            decode_step(self.cache, self.step_k.view(B, Q, w.n_kv_heads, w.head_dim),
+                        self.step_v.view(B, Q, w.n_kv_heads, w.head_dim), self.q, self.page_table, self.seq_lens,
+                        w.max_seq_len, self.out, self.workspace, w.sm_scale, stream=stream)
+            return
         kv_append(self.cache, self.step_k, self.step_v, self.step_slots, stream=stream)
         decode_attn(self.cache, self.q, self.page_table, self.seq_lens, w.max_seq_len, self.out, self.workspace,
                     w.sm_scale, stream=stream)
@@ -80,8 +90,8 @@ class StepResult:
     initial_v_pool: np.ndarray | None = None
 
 
-def run_workload(w, fill_seed: int | None = None, want_pools: bool = False) -> StepResult:
-    """Upload, fill, run one step, copy everything back."""
+def run_workload(w, fill_seed: int | None = None, want_pools: bool = False, fused: bool = False) -> StepResult:
+    """Upload, fill, run one step (fused: through memra_decode_step), copy everything back."""
     import torch
     init_k = init_v = None
     dw = upload(w, fill_seed=fill_seed)
@@ -90,7 +100,7 @@ def run_workload(w, fill_seed: int | None = None, want_pools: bool = False) -> S
         g = torch.Generator(device="cpu").manual_seed(fill_seed)
         init_k = torch.randint(0, 256, dw.cache.k_pool.shape, dtype=torch.uint8, generator=g).numpy()
         init_v = torch.randint(0, 256, dw.cache.v_pool.shape, dtype=torch.uint8, generator=g).numpy()
-    dw.step()
+    dw.step(fused=fused)
     flags = read_status(dw.cache)
     torch.cuda.synchronize()
     out = dw.out.cpu().numpy()

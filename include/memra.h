@@ -187,6 +187,29 @@ int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_le
                               int32_t head_dim, const void *workspace, size_t workspace_bytes, void *out,
                               void *stream);
 
+/* One decode step in a single split-K pass: quantize-append of the step's new
+ * rows fused into the attention that reads them (the write and read sides of
+ * the memra README's paged, block-quantized cache, "Speculative decoding" for
+ * q_len > 1).  Same results as memra_kv_append of the rows at slots
+ * page_table[b][pos/16]*16 + pos%16, pos = seq_lens[b]-q_len .. seq_lens[b]-1,
+ * followed by memra_decode_attn; the pool bytes are bit-identical.
+ *   k_new, v_new  device fp16 [batch][q_len][n_kv_heads][head_dim], 16-byte
+ *                 aligned: the K / V rows of the q_len new tokens, in position
+ *                 order
+ *   other arguments as memra_decode_attn; max_seq_len >= q_len.
+ * Each new row is stored by the CTA whose split holds its position, before
+ * that CTA copies the page in, so no other launch is needed.  The pages that
+ * receive new rows must belong to one sequence of the batch (a page shared by
+ * two sequences, e.g. a shared prefix, is read-only here).  Rows whose page
+ * id is out of range are skipped (MEMRA_DEVERR_BAD_PAGE); a sequence shorter
+ * than q_len stores only the rows with a position >= 0 and sets
+ * MEMRA_DEVERR_BAD_SEQ_LEN. */
+int memra_decode_step(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                      const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                      int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                      int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+                      void *stream);
+
 /* Fixed size of the device array that memra_decode_attn_noalloc uses for the
  * split-K partials (held on every device that calls it, until exit). */
 #define MEMRA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -337,3 +337,116 @@ def test_long_sequence_with_wide_splits():
     res = run(w, want_pools=False)
     assert res.flags == 0
     assert_out_close(w, res, attention.reference(w))
+
+
+# ------------------------------------------- fused append + attention step --
+# memra_decode_step stores the step's rows from inside the split kernel.  Its
+# pools must match the oracle's bit for bit and its outputs the two-call path
+# (memra_kv_append + memra_decode_attn) byte for byte: both read the same
+# quantized bytes through the same arithmetic.
+
+def run_fused(w, fill_seed=1, want_pools=True):
+    from decode_attention_block_memra_gb300.runner import run_workload
+    return run_workload(w, fill_seed=fill_seed, want_pools=want_pools, fused=True)
+
+
+def assert_fused_matches(w, want_pools=True):
+    res = run_fused(w, want_pools=want_pools)
+    assert res.flags == 0
+    if want_pools:
+        assert_pools_exact(w, res)
+    two_call = run(w, want_pools=False)
+    assert np.array_equal(res.out.view(np.uint16), two_call.out.view(np.uint16)), "fused and two-call outputs differ"
+    return res
+
+
+def test_fused_step_tiny():
+    w = W.tiny()
+    res = assert_fused_matches(w)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kf,vf", FORMAT_PAIRS)
+def test_fused_step_formats(kf, vf, D):
+    w = W.random_case(2000 + D + 7 * FORMAT_PAIRS.index((kf, vf)), batch=3, q_len=2, n_heads=16, n_kv_heads=2,
+                      head_dim=D, k_fmt=kf, v_fmt=vf, ctx=(5, 2600))
+    res = assert_fused_matches(w)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("q_len,n_heads,n_kv_heads,D,seq_lens", [
+    (1, 8, 1, 128, [1]),                  # the only key is the new one
+    (1, 8, 1, 128, [17, 16, 1025]),       # new row opens a page / closes a page / opens a split
+    (4, 32, 4, 128, [1026, 1030, 4]),     # verify rows cross the split boundary at 1,024; whole sequence new
+    (6, 8, 2, 128, [8000, 1027]),         # new rows deep in a long split (beyond the first ring fill)
+    (8, 64, 8, 128, [700, 2049]),         # 64 rows per KV head
+    (4, 16, 2, 256, [33, 1100]),          # D 256: 32 lanes per stored row
+])
+def test_fused_step_positions(q_len, n_heads, n_kv_heads, D, seq_lens):
+    w = W.make_workload("fused_pos", batch=len(seq_lens), q_len=q_len, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                        head_dim=D, k_fmt="q8_0", v_fmt="q5_1", seed=sum(seq_lens) + q_len, seq_lens=seq_lens,
+                        permute_pages=True, extra_pages=3)
+    res = assert_fused_matches(w)
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_fused_step_shared_prefix():
+    w = W.make_workload("sp_fused", batch=4, q_len=2, n_heads=16, n_kv_heads=2, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=21, seq_lens=[1100, 1026, 2100, 1040], shared_prefix=1024)
+    res = assert_fused_matches(w)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("kf,vf", [("q8_0", "q5_1"), ("q8_0", "q4_0")])
+def test_fused_step_adversarial_rows(kf, vf):
+    """The fused store is bit-exact on rounding ties, subnormal scales and extreme ranges."""
+    w = W.random_case(505, batch=4, q_len=8, n_heads=16, n_kv_heads=2, head_dim=128, k_fmt=kf, v_fmt=vf,
+                      ctx=(8, 700))
+    rng = np.random.default_rng(6)
+    n = w.step_rows.size * w.n_kv_heads
+    w.k_rows[w.step_rows] = _adversarial_rows(rng, n, 128).reshape(w.step_rows.size, w.n_kv_heads, 128)
+    w.v_rows[w.step_rows] = _adversarial_rows(rng, n, 128).reshape(w.step_rows.size, w.n_kv_heads, 128)
+    res = run_fused(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert np.isfinite(res.out.astype(np.float32)).all()
+
+
+def test_fused_step_full_size_long_context():
+    w = W.WORKLOADS["long_context"]()
+    cache = attention.quantize_cache(w)
+    res = run_fused(w)
+    assert res.flags == 0
+    rows = np.union1d(np.random.default_rng(3).choice(w.slots.size, 5000, replace=False), w.step_rows)
+    assert_rows_exact(w, res, rows, cache)
+    assert_out_close(w, res, attention.reference(w, cache=cache))
+
+
+def test_fused_step_bad_page_and_validation():
+    import decode_attention_block_memra_gb300 as memra
+    w = W.random_case(13, batch=2, q_len=2, n_heads=8, n_kv_heads=2, ctx=(300, 900))
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w, fill_seed=4)
+    T0 = int(w.seq_lens[0])
+    dw.page_table[0, (T0 - 1) // 16] = w.num_pages + 5      # the page of sequence 0's last new row
+    before = dw.cache.k_pool.clone()
+    B, Q = w.batch, w.q_len
+    k_new = dw.step_k.view(B, Q, w.n_kv_heads, w.head_dim)
+    v_new = dw.step_v.view(B, Q, w.n_kv_heads, w.head_dim)
+    memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
+                      w.sm_scale)
+    assert memra.read_status(dw.cache) & memra.DEVERR_BAD_PAGE
+    assert torch.isfinite(dw.out.float()).all()
+    # only rows of the step were stored: every changed byte lies in a page that holds a step row
+    changed = (before != dw.cache.k_pool).view(w.num_pages, -1).any(dim=1).nonzero().flatten().cpu().numpy()
+    step_pages = set((w.slots[w.step_rows] // 16).tolist())
+    assert set(changed.tolist()) <= step_pages
+    with pytest.raises(memra.MemraError) as e:                 # misaligned rows
+        memra.decode_step(dw.cache, k_new.view(-1)[1:], v_new, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len,
+                          dw.out, dw.workspace, w.sm_scale)
+    assert e.value.status == 1
+    with pytest.raises(memra.MemraError) as e:                 # max_seq_len below q_len
+        memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, 1, dw.out, dw.workspace,
+                          w.sm_scale)
+    assert e.value.status == 1
