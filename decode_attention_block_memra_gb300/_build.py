@@ -16,9 +16,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libmemra.so")
 
-SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128_nt1.cu", "decode_d128_nt2.cu",
-           "decode_d256_nt1.cu", "noalloc.cu"]
-HEADERS = ["memra_device.cuh", "decode_kernel.cuh"]
+SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128.cu", "decode_d256.cu", "noalloc.cu"]
+HEADERS = ["memra_device.cuh", "decode_kernel.cuh", "kv_quant.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

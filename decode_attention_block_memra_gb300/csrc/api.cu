@@ -37,7 +37,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MEMRA_OK : MEMRA_ERR_
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
-  int nt, ngrp, qg, nsplit_max, num_stages, ctas_per_sm;
+  int ngh, ngh_q, nsplit_max, num_stages, ctas_per_sm;
   size_t smem;
 };
 
@@ -60,48 +60,35 @@ int split_target(const Plan &pl, int n_kv_heads) {
   return t > 0 ? t : 1;
 }
 
-int warps_for(int D, int nt) { return (D == 128 && nt == 1) ? kWarpsFor<128, 1> : kWarpsFor<256, 1>; }
+int warps_for(int D) { return D == 128 ? kWarpsFor<128> : kWarpsFor<256>; }
 
-size_t merge_bytes(int D, int nt) {
-  const size_t rows_w = 8 * nt, nb = D / 32;
-  const size_t w = warps_for(D, nt);
+size_t merge_bytes(int D) {
+  const size_t rows_w = 8, nb = D / 32;
+  const size_t w = warps_for(D);
   return (w * rows_w * D + 2 * w * rows_w + w * rows_w * nb) * 4;
 }
 
-// Row tiling and pipeline depth.  Rows (q_len x group) are cut into groups of
-// 8*nt rows per warp; the 4 consumer warps split into row groups x page lanes.
+// CTAs per (split, KV head, sequence) and pipeline depth.  Every query
+// position and every group of 8 query heads of a KV head gets its own CTA
+// (8 rows, one per MMA column), planned from the position's own length.
 int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan *pl) {
-  const int qg = q_len * group;
-  int nt, ngrp;
-  if (qg <= 8) {
-    nt = 1;
-    ngrp = 1;
-  } else if (D == 128) {
-    nt = 2;
-    ngrp = static_cast<int>(ceil_div(qg, 16));
-  } else {
-    nt = 1;
-    ngrp = static_cast<int>(ceil_div(qg, 8));
-  }
-  if (ngrp == 3) ngrp = 4;
-  const int W = warps_for(D, nt);
-  if (ngrp > W) return MEMRA_ERR_UNSUPPORTED;
+  if (q_len > MEMRA_MAX_Q_LEN || group > MEMRA_MAX_GROUP) return MEMRA_ERR_UNSUPPORTED;
+  const int W = warps_for(D);
   // Pipeline depth: as many 16-token pages in flight as fit beside the other
   // CTA of the SM, in steps of the warp count so that page i and page
   // i + depth meet the same warp.
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
   const int ctas_per_sm = 2;
-  const size_t qbytes = static_cast<size_t>(W) * nt * (D / 32) * 512;     // warp-private Q fragments
+  const size_t qbytes = static_cast<size_t>(W) * (D / 32) * 512;     // warp-private Q fragments
   const size_t budget = (226 * 1024) / ctas_per_sm - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
   int ns = static_cast<int>(budget / stage) & ~(W - 1);
   if (ns > 32) ns = 32;
   if (ns < W) ns = W;
   size_t region = stage * ns;
-  const size_t mb = merge_bytes(D, nt);
+  const size_t mb = merge_bytes(D);
   if (mb > region) region = mb;
-  pl->nt = nt;
-  pl->ngrp = ngrp;
-  pl->qg = qg;
+  pl->ngh = static_cast<int>(ceil_div(group, 8));
+  pl->ngh_q = pl->ngh * q_len;
   pl->nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
   pl->num_stages = ns;
   pl->ctas_per_sm = ctas_per_sm;
@@ -139,6 +126,9 @@ int check_decode(const DecodeArgs &a) {
     return MEMRA_ERR_INVALID_ARG;
   if (a.n_kv_heads != a.cache->n_kv_heads || a.head_dim != a.cache->head_dim) return MEMRA_ERR_INVALID_ARG;
   if (a.n_heads % a.n_kv_heads) return MEMRA_ERR_INVALID_ARG;
+  if (a.q_len > MEMRA_MAX_Q_LEN || a.n_heads / a.n_kv_heads > MEMRA_MAX_GROUP || a.batch > 65535 ||
+      a.n_kv_heads > 65535)
+    return MEMRA_ERR_UNSUPPORTED;
   if (!std::isfinite(a.sm_scale)) return MEMRA_ERR_INVALID_ARG;
   if (a.batch == 0) return MEMRA_OK;
   if (!a.q || !a.page_table || !a.seq_lens || !a.out) return MEMRA_ERR_INVALID_ARG;
@@ -181,10 +171,10 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.q_len = a.q_len;
   p.n_heads = a.n_heads;
   p.group = group;
-  p.qg = pl.qg;
+  p.ngh = pl.ngh;
+  p.ngh_q = pl.ngh_q;
   p.nsplit_max = pl.nsplit_max;
   p.num_stages = pl.num_stages;
-  p.ngrp = pl.ngrp;
   p.split_target = split_target(pl, c.n_kv_heads);
   const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
@@ -193,13 +183,12 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   // no sequence has more splits than min(ceil(T/1024), max(target, ceil(T/8192)))
   const int64_t most = std::min<int64_t>(pl.nsplit_max, std::max<int64_t>(p.split_target,
                                                                           ceil_div(a.max_seq_len, kSplitTokensMax)));
-  const dim3 grid(static_cast<unsigned>(most), static_cast<unsigned>(c.n_kv_heads), static_cast<unsigned>(a.batch));
-  cudaError_t e;
-  if (a.head_dim == 128)
-    e = pl.nt == 1 ? launch_decode_d128_nt1(c.k_fmt, c.v_fmt, p, grid, pl.smem, st)
-                   : launch_decode_d128_nt2(c.k_fmt, c.v_fmt, p, grid, pl.smem, st);
-  else
-    e = launch_decode_d256_nt1(c.k_fmt, c.v_fmt, p, grid, pl.smem, st);
+  // x: split-major, then query position and head group (the CTAs that read
+  // the same pages run side by side and share them through L2)
+  const dim3 grid(static_cast<unsigned>(most * pl.ngh_q), static_cast<unsigned>(c.n_kv_heads),
+                  static_cast<unsigned>(a.batch));
+  const cudaError_t e = a.head_dim == 128 ? launch_decode_d128(c.k_fmt, c.v_fmt, p, grid, pl.smem, st)
+                                          : launch_decode_d256(c.k_fmt, c.v_fmt, p, grid, pl.smem, st);
   return cuda_status(e);
 }
 

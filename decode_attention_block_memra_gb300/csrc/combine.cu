@@ -1,7 +1,7 @@
 // K3: log-sum-exp combine of the split-K partials.
 //
-// For a query row whose sequence spans several splits, the split
-// kernel left (o_s = O_s / l_s, lse_s = m_s + log2 l_s) per split.  The exact
+// For a query row whose visible keys (those up to its own position) span
+// several splits, the split kernel left (o_s = O_s / l_s, lse_s = m_s + log2 l_s) per split.  The exact
 // merge is  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max lse_s
 // (splits with no visible key have lse = -inf and weight 0).  One CTA per
 // row with up to 16 warps; warp w takes splits w, w+16, ... (eight in flight),
@@ -29,15 +29,18 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int b = row / (p.q_len * p.n_heads);
-  const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status, false);
-  const int C = split_tokens(T, p.split_target);
-  const int ns = (T + C - 1) / C;
-  if (ns == 1) return;                              // the split kernel wrote this row
+  const int qi = (row / p.n_heads) % p.q_len;
+  // keys visible to this row's position (its own split plan, as in the split kernel)
+  const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status, false) - p.q_len +
+                qi + 1;
   __half *dst = p.out + static_cast<size_t>(row) * D;
-  if (ns == 0) {                                    // empty sequence: zeros
+  if (T <= 0) {                                     // no visible key: zeros
     for (int j = threadIdx.x; j < D; j += blockDim.x) dst[j] = __float2half(0.f);
     return;
   }
+  const int C = split_tokens(T, p.split_target);
+  const int ns = (T + C - 1) / C;
+  if (ns == 1) return;                              // the split kernel wrote this row
   const float *lse = p.lse_part + static_cast<size_t>(row) * p.nsplit_max;
   const float *op = p.o_part + static_cast<size_t>(row) * p.nsplit_max * D + lane * PER;
   float acc[PER];

@@ -1,0 +1,11 @@
+// Instantiations of the split-K decode kernel for head_dim 256 (all six K/V
+// format pairs); one translation unit per head_dim so they compile in parallel.
+#include "decode_kernel.cuh"
+
+namespace memra {
+
+cudaError_t launch_decode_d256(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
+  return dispatch_formats<256>(kf, vf, p, grid, smem, st);
+}
+
+}  // namespace memra

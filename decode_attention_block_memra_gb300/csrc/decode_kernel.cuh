@@ -1,38 +1,49 @@
 // K2: split-K flash-decoding over the block-quantized paged KV cache.
 //
-// What it computes: for one (sequence, KV head, split of C(T) tokens), the
-// partial softmax(q K^T * scale) V over the split's keys for all the query
-// rows that read this KV head (the head's GQA group times q_len, causal among
-// the q_len new tokens), as (o = O / l, lse = m + log2 l).  The KV formats are
-// the memra-bench card's knobs (section "drafts/kf4/ - archived experiment");
-// plain decode and MTP verify are the memra README's "Speculative decoding"
-// item; the 262,144-token contexts its "Long context and larger models" item.
+// What it computes: for one (sequence, KV head, query position, group of up
+// to 8 query heads, split of C(T) tokens), the partial softmax(q K^T * scale) V
+// over the split's keys, as (o = O / l, lse = m + log2 l); T is the number of
+// keys the position sees (causal among the q_len new tokens).  The KV formats
+// are the memra-bench card's knobs (section "drafts/kf4/ - archived
+// experiment"); plain decode and MTP verify are the memra README's
+// "Speculative decoding" item; the 262,144-token contexts its "Long context
+// and larger models" item.
 //
-// How (one CTA = 4 warps):
-//  * Warp w takes every R-th page of the split (R = 4 / row groups) and owns
-//    the ring stages of those pages.  The page lane's first warp streams each
-//    page's K and V segments (one contiguous bulk copy each, 16-byte aligned,
-//    evict-first in L2) into its stages, `num_stages` pages ahead, completing
-//    on per-stage mbarriers, and refills a stage as soon as it is read.  Per page:
-//    S^T[16 tokens x 8 rows] = K^ Q^T on the tensor cores (m16n8k16, fp16 in,
-//    fp32 out) with the K codes converted to fp16 in registers; the q8_0 block
-//    scale multiplies each 32-element block's partial sum, so K^ is exact.
-//    Online softmax in the fp32 accumulators (row max over the 8 token lanes
-//    by xor-shuffles), P transposed in registers (movmatrix) into the B
-//    operand, then O^T[D x rows] += V^T P^T with the V codes converted in
-//    registers and the per-token block scale folded into P; q5_1's +m term is
-//    one extra MMA (blocks x tokens) * P^T.
+// Every query position is planned as its own decode problem: its split size
+// C(T) comes from its own T, its CTAs see exactly the keys a q_len = 1 call at
+// that position sees, and nothing in a row's arithmetic depends on the other
+// rows of the call.  So verify rows are byte-identical to plain decode at the
+// same positions (the README's single numeric class for speculative decode).
+// The CTAs of one split's positions are neighbours in the grid and read the
+// same pages, so L2 serves all but the first read.
+//
+// How (one CTA = 8 warps at head_dim 128, 4 at 256, 2 CTAs per SM):
+//  * Warp w takes pages w, w + W, ... of the split, issues its own pages'
+//    copies (one contiguous bulk copy each for the K and V segments, 16-byte
+//    aligned, evict-first in L2) `num_stages` pages ahead into its own ring
+//    stages, completing on per-stage mbarriers, and refills a stage once read.
+//    Per page: S^T[16 tokens x 8 rows] = K^ Q^T on the tensor cores
+//    (m16n8k16, fp16 in, fp32 out) with the K codes converted to fp16 in
+//    registers; the q8_0 block scale multiplies each 32-element block's
+//    partial sum, so K^ is exact.  Online softmax in the fp32 accumulators
+//    (row max over the 8 token lanes by xor-shuffles), P transposed in
+//    registers (movmatrix) into the B operand, then O^T[D x rows] += V^T P^T
+//    with the V codes converted in registers and the per-token block scale
+//    folded into P; q5_1's +m term is one extra MMA (blocks x tokens) * P^T.
 //  * q8_0 K codes are stored biased (q + 128) and become fp16 1152 + q with
 //    one byte permute per pair; one more MMA per page, with the block scales
 //    as A and -1152 * sum(Q) as B (fp16 hi + lo), takes the bias out.
 //  * The reference maximum of a row moves only when a score passes it by more
 //    than 2 (log2 units), so O and l are rescaled only then.
-//  * At the end the consumer warps merge their (m, l, O) through shared
-//    memory; a split that covers the whole sequence writes fp16 output,
+//  * At the end the warps merge their (m, l, O) through shared memory; a
+//    split that covers all of the position's keys writes fp16 output,
 //    otherwise an fp32 partial for the combine kernel.
+//  * Fused append (memra_decode_step): the step's new K/V rows that the CTA
+//    sees are quantized and stored into their pages before those pages are
+//    copied in.
 // Every wait is bounded (MEMRA_DEVERR_TIMEOUT); bad page ids are skipped
-// (MEMRA_DEVERR_BAD_PAGE); tokens past seq_len never reach the result, even if
-// their bytes are garbage.
+// (MEMRA_DEVERR_BAD_PAGE); keys past T never reach the result, even if their
+// bytes are garbage.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -58,8 +69,10 @@ struct DecodeParams {
   // stored at positions seq_len - q_len .. seq_len - 1 before they are read.
   const __half *k_new;
   const __half *v_new;
-  int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group, qg;
-  int nsplit_max, num_stages, ngrp, split_target;
+  int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group;
+  int ngh;            // groups of 8 query heads per KV head: ceil(group / 8)
+  int ngh_q;          // CTAs per (split, KV head, sequence): q_len * ngh
+  int nsplit_max, num_stages, split_target;
   float scale_log2, v_scale, k_scale;
 };
 
@@ -76,16 +89,15 @@ cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
 cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
                              cudaStream_t stream);
 
-// Warps per CTA: 8 at head_dim 128 with 8 query rows per warp (fewer pages
-// per warp for short sequences; 2 CTAs/SM still give 16 warps), else 4.
-template <int D, int NT>
-constexpr int kWarpsFor = (D == 128 && NT == 1) ? 8 : 4;
+// Warps (page lanes) per CTA: 8 at head_dim 128, 4 at 256; 2 CTAs/SM.
+template <int D>
+constexpr int kWarpsFor = D == 128 ? 8 : 4;
 constexpr int kMaxWarps = 8;
 
-template <int D, int NT>
+template <int D>
 struct MergeLayout {
-  static constexpr int kW = kWarpsFor<D, NT>;
-  static constexpr int kRowsW = 8 * NT;
+  static constexpr int kW = kWarpsFor<D>;
+  static constexpr int kRowsW = 8;
   static constexpr int kNb = D / 32;
   static constexpr int kO = kW * kRowsW * D;          // floats
   static constexpr int kM = kW * kRowsW;
@@ -120,15 +132,16 @@ __device__ __forceinline__ uint32_t shift_const(uint32_t x) {
   else return x << (-SH);
 }
 
-template <int D, int KF, int VF, int NT>
-__global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
+template <int D, int KF, int VF>
+__global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
     decode_split_kernel(const DecodeParams p) {
+  constexpr int NT = 1;                       // one n-tile of 8 query rows
   constexpr int NB = D / 32;
   constexpr int KSEG = k_seg_bytes(KF, D);
   constexpr int VSEG = v_seg_bytes(VF, D);
   constexpr int STAGE = KSEG + VSEG;
-  using ML = MergeLayout<D, NT>;
-  constexpr int kWarps = kWarpsFor<D, NT>;
+  using ML = MergeLayout<D>;
+  constexpr int kWarps = kWarpsFor<D>;
   constexpr int kThreads = kWarps * 32;
   constexpr int ROWS_W = ML::kRowsW;
   constexpr bool kQ5 = VF == MEMRA_KV_Q5_1;
@@ -139,36 +152,39 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
 
   extern __shared__ __align__(128) uint8_t smem[];
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status,
-                              split == 0 && kvh == 0 && threadIdx.x == 0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NS = p.num_stages;                  // a multiple of the warp count: page i and i + NS share a warp
+  const int region = max(NS * STAGE, ML::kBytes);
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t full0 = ring + region;
+  int *pid_s = reinterpret_cast<int *>(smem + region + 16 * NS);   // page ids of this split, -1 = bad
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
+    fence_barrier_init();
+  }
+  grid_dependency_wait();       // inputs written by the launch before this one have landed
+
+  // This CTA: query position qi of sequence b and query heads 8 hg .. 8 hg + 7
+  // of KV head kvh's group, over the keys visible to position qi (the first
+  // T of the sequence), split s of that range.  Each query position is its
+  // own decode problem, planned from its own length exactly as a q_len = 1
+  // call at that position would be.
+  const int vr = blockIdx.x % p.ngh_q, split = blockIdx.x / p.ngh_q;
+  const int qi = vr / p.ngh, hg = vr % p.ngh;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status,
+                                 blockIdx.x == 0 && kvh == 0 && tid == 0);
+  const int T = Tseq - p.q_len + qi + 1;
+  if (T <= 0) return;
   const int C = split_tokens(T, p.split_target);
   const int tok0 = split * C;
   if (tok0 >= T) return;
   const int npages = (min(T, tok0 + C) - tok0 + kPage - 1) / kPage;
   const int nsplit_b = (T + C - 1) / C;
+  const int nrows = min(8, p.group - 8 * hg);   // query heads of this CTA
+  const int R = kWarps;                         // page lanes: warp r takes pages r, r + R, ...
+  const int r = warp;
 
-  const int NS = p.num_stages;                  // a multiple of 4, so page i and i + NS share a warp
-  const int region = max(NS * STAGE, ML::kBytes);
-  const uint32_t ring = smem_addr(smem);
-  const uint32_t full0 = ring + region;
-  const uint32_t empty0 = full0 + 8 * NS;
-  int *pid_s = reinterpret_cast<int *>(smem + region + 16 * NS);   // page ids of this split, -1 = bad
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ngrp = p.ngrp;
-  const int R = kWarps / ngrp;                  // page lanes
-  const int gr = warp % ngrp, r = warp / ngrp;  // row group, page lane
-  const bool issuer = gr == 0;                  // one warp per page lane issues its copies
-
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, ngrp);
-    }
-    fence_barrier_init();
-  }
-  grid_dependency_wait();       // the append that precedes this launch has landed
   {
     const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages + tok0 / kPage;
     for (int i = tid; i < npages; i += kThreads) {
@@ -198,31 +214,30 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
       mbar_arrive(bar);
     }
   };
-  // New tokens of this step that fall in this split (fused append only): their
-  // pages [app_lo, app_hi] are copied in only after the rows are stored.
-  const int app_pos0 = max(max(T - p.q_len, tok0), 0);
+  // New tokens of this step that this CTA sees and that fall in this split
+  // (fused append only): their pages [app_lo, app_hi] are copied in only after
+  // the rows are stored.  CTAs of later positions store the same rows again
+  // (same bytes); each orders its own stores before its own copies.
+  const int app_pos0 = max(max(Tseq - p.q_len, tok0), 0);
   const int app_n = p.k_new ? max(min(T, tok0 + C) - app_pos0, 0) : 0;
   const int app_lo = app_n ? app_pos0 / kPage - tok0 / kPage : npages;
   const int app_hi = app_n ? (app_pos0 + app_n - 1) / kPage - tok0 / kPage : -1;
-  if (issuer && lane == 0) {
+  if (lane == 0) {
     for (int i = r; i < min(NS, npages); i += R)
       if (i < app_lo || i > app_hi) issue(i, i);
   }
 
   const int g = lane >> 2, c = lane & 3;
-  const int row_base = gr * ROWS_W;
   // Q^T fragments live in shared memory (warp-private, fragment order: one
-  // conflict-free 16-byte load per block and n-tile), not in 16+ registers.
+  // conflict-free 16-byte load per block), not in 16+ registers.
   const uint32_t qsm = smem_addr(smem + region + 16 * NS + 4 * kSplitPagesMax) + warp * (NT * NB * 512);
 
-  // Q^T fragments (B operand of S^T = K^ Q^T): row 8n+g, dims 32bb+8c..+7.
+  // Q^T fragments (B operand of S^T = K^ Q^T): row g, dims 32bb+8c..+7.
   uint4 qf[NT][NB];
-  int lastv[NT][2];     // last visible key of the thread's rows 8n+2c+u
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
-    const int nr = row_base + 8 * n + g;
-    if (nr < p.qg) {
-      const int qi = nr / p.group, head = kvh * p.group + nr % p.group;
+    if (g < nrows) {
+      const int head = kvh * p.group + 8 * hg + g;
       const uint4 *src = reinterpret_cast<const uint4 *>(
           p.q + ((static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head) * D + 8 * c);
 #pragma unroll
@@ -231,13 +246,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
 #pragma unroll
       for (int bb = 0; bb < NB; ++bb) qf[n][bb] = make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int row = row_base + 8 * n + 2 * c + u;
-      lastv[n][u] = row < p.qg ? T - p.q_len + row / p.group : 0x7fffffff;
-    }
   }
-  const int min_last = T - p.q_len;    // last key every real row sees
 
   // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q,
   // so block b's raw product is acc_b = sum_j q_j Q_j + 1152 sum_j Q_j.  The
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
     const QuantTarget dst{const_cast<uint8_t *>(p.k_pool), const_cast<uint8_t *>(p.v_pool), p.n_kv_heads, KF, VF,
                           p.k_scale, p.v_scale};
     const int l = tid % kLanesRow;
-    const int first_new = T - p.q_len;       // position of new token 0
+    const int first_new = Tseq - p.q_len;    // position of new token 0
     for (int j0 = 0; j0 < app_n; j0 += kRowsPass) {
       const int j = j0 + tid / kLanesRow;
       const int pos = app_pos0 + j;
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
     }
     fence_proxy_async_global();
     __syncthreads();
-    if (issuer && lane == 0) {
+    if (lane == 0) {
       for (int i = r; i < min(NS, npages); i += R)
         if (i >= app_lo && i <= app_hi) issue(i, i);
     }
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
       // Pages wholly inside every row's visible range (all but the last one or
       // two of a sequence) take a path without any masking code.
       const int pos_first = tok0 + i * kPage;
-      const bool plain = pos_first + kPage - 1 <= min_last && pos_first + kPage <= T;
+      const bool plain = pos_first + kPage <= T;
       auto page = [&](auto tail) {
         const uint32_t ka = ring + s * STAGE;
         const uint32_t va = ka + KSEG;
@@ -439,10 +448,10 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
             for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
           if (masked) {
             const int t0 = pos0 + g, t1 = pos0 + g + 8;
-            s4[n][0] = t0 <= lastv[n][0] ? s4[n][0] : -INFINITY;
-            s4[n][1] = t0 <= lastv[n][1] ? s4[n][1] : -INFINITY;
-            s4[n][2] = t1 <= lastv[n][0] ? s4[n][2] : -INFINITY;
-            s4[n][3] = t1 <= lastv[n][1] ? s4[n][3] : -INFINITY;
+            s4[n][0] = t0 < T ? s4[n][0] : -INFINITY;
+            s4[n][1] = t0 < T ? s4[n][1] : -INFINITY;
+            s4[n][2] = t1 < T ? s4[n][2] : -INFINITY;
+            s4[n][3] = t1 < T ? s4[n][3] : -INFINITY;
           }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -614,16 +623,10 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
         page(std::true_type{});
     }
     __syncwarp();
-    // Release the stage; the page lane's issuing warp refills it with page i + NS
-    // once every row group has released it.
-    if (lane == 0) {
-      if (ngrp > 1) mbar_arrive(empty0 + 8 * s);       // other row groups read this stage too
-      if (issuer && i + NS < npages) {
-        if (ngrp == 1 || mbar_wait_bounded(empty0 + 8 * s, par, p.status)) {
-          fence_proxy_async();
-          issue(i + NS, s);
-        }
-      }
+    // The stage is read: refill it with page i + NS (this warp's next page there).
+    if (lane == 0 && i + NS < npages) {
+      fence_proxy_async();
+      issue(i + NS, s);
     }
     s += R;
     if (s >= NS) {
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
   }
   // A wait that gave up: stay until this lane's copies in flight have landed
   // (bounded), so no bulk copy outlives the CTA's shared memory.
-  if (stop_at >= 0 && issuer && lane == 0) {
+  if (stop_at >= 0 && lane == 0) {
     for (int j = stop_at; j < min(stop_at + NS, npages); j += R) {
       if (!mbar_wait_bounded(full0 + 8 * (j % NS), (j / NS) & 1, p.status)) break;
     }
@@ -686,17 +689,16 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
   __syncthreads();
 
   const float vscale = VF == MEMRA_KV_FP8_E4M3 ? p.v_scale : 1.f;
-  for (int item = tid; item < p.qg * (D / 4); item += kThreads) {
-    const int nrow = item / (D / 4);
+  for (int item = tid; item < nrows * (D / 4); item += kThreads) {
+    const int lr = item / (D / 4);
     const int j4 = (item % (D / 4)) * 4;
-    const int grp = nrow / ROWS_W, lr = nrow % ROWS_W;
     float M = -INFINITY;
-    for (int rr = 0; rr < R; ++rr) M = fmaxf(M, mm[(rr * ngrp + grp) * ROWS_W + lr]);
+    for (int rr = 0; rr < R; ++rr) M = fmaxf(M, mm[rr * ROWS_W + lr]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     if (M != -INFINITY) {
       for (int rr = 0; rr < R; ++rr) {
-        const int wr = (rr * ngrp + grp) * ROWS_W + lr;
+        const int wr = rr * ROWS_W + lr;
         const float wgt = fast_exp2(mm[wr] - M);
         L = fmaf(wgt, ml[wr], L);
         const float4 x = *reinterpret_cast<const float4 *>(mo + wr * D + j4);
@@ -709,7 +711,7 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
     }
     const float inv = L > 0.f ? vscale / L : 0.f;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-    const int qi = nrow / p.group, head = kvh * p.group + nrow % p.group;
+    const int head = kvh * p.group + 8 * hg + lr;
     const size_t rowid = (static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head;
     if (nsplit_b == 1) {
       uint2 h;
@@ -725,33 +727,32 @@ __global__ void __launch_bounds__(kWarpsFor<D, NT> * 32, 2)
   allow_dependent_launch();
 }
 
-// One dispatcher per translation unit (head_dim, rows per warp).
-cudaError_t launch_decode_d128_nt1(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
-cudaError_t launch_decode_d128_nt2(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
-cudaError_t launch_decode_d256_nt1(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
+// One dispatcher per translation unit (head_dim).
+cudaError_t launch_decode_d128(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_decode_d256(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st);
 
-template <int D, int KF, int VF, int NT>
+template <int D, int KF, int VF>
 cudaError_t launch_one(const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
   static bool configured = false;   // per instantiation; attribute is per device function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, KF, VF, NT>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, KF, VF>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(decode_split_kernel<D, KF, VF, NT>, grid, dim3(kWarpsFor<D, NT> * 32), smem, st, p);
+  return launch_pdl(decode_split_kernel<D, KF, VF>, grid, dim3(kWarpsFor<D> * 32), smem, st, p);
 }
 
-template <int D, int NT>
+template <int D>
 cudaError_t dispatch_formats(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
   if (kf == MEMRA_KV_Q8_0) {
-    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q5_1, NT>(p, grid, smem, st);
-    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q4_0, NT>(p, grid, smem, st);
-    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_FP8_E4M3, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q5_1>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q4_0>(p, grid, smem, st);
+    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_FP8_E4M3>(p, grid, smem, st);
   } else if (kf == MEMRA_KV_FP8_E4M3) {
-    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q5_1, NT>(p, grid, smem, st);
-    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q4_0, NT>(p, grid, smem, st);
-    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_FP8_E4M3, NT>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q5_1>(p, grid, smem, st);
+    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q4_0>(p, grid, smem, st);
+    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_FP8_E4M3>(p, grid, smem, st);
   }
   return cudaErrorInvalidValue;
 }

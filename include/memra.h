@@ -109,6 +109,10 @@ typedef enum {
  * own length and the device, never on the rest of the batch: a sequence's
  * result bytes are the same alone or batched. */
 #define MEMRA_PAGE_SIZE 16
+/* Largest q_len (new tokens per sequence: 1 + draft tokens) and largest GQA
+ * group n_heads / n_kv_heads that the decode calls take. */
+#define MEMRA_MAX_Q_LEN 16
+#define MEMRA_MAX_GROUP 128
 #define MEMRA_SPLIT_TOKENS 1024
 #define MEMRA_SPLIT_TOKENS_MAX 8192
 
@@ -162,11 +166,18 @@ size_t memra_decode_attn_workspace_bytes(int32_t batch, int32_t q_len, int32_t n
  *                q_len new tokens (append them first with memra_kv_append)
  *   max_seq_len  host upper bound of seq_lens (sizes the split grid)
  *   n_kv_heads, head_dim must equal the cache's; n_heads % n_kv_heads == 0;
- *   q_len*(n_heads/n_kv_heads) <= 64 (head_dim 128) or <= 32 (head_dim 256)
+ *   q_len <= MEMRA_MAX_Q_LEN, n_heads/n_kv_heads <= MEMRA_MAX_GROUP, batch and
+ *   n_kv_heads <= 65535 (else MEMRA_ERR_UNSUPPORTED)
  *   sm_scale     softmax scale (1/sqrt(head_dim) for standard attention)
  *   workspace    device, >= memra_decode_attn_workspace_bytes(...) bytes
  *   out          device fp16 [batch][q_len][n_heads][head_dim]
- * batch == 0 is a no-op.  A sequence of length 0 yields zeros. */
+ * Query row i of sequence b sits at position seq_lens[b] - q_len + i and sees
+ * keys 0 .. that position.  Each row's result depends only on its visible
+ * keys, its query and the device: a verify row (q_len > 1) has the same
+ * bytes as a q_len = 1 call at that position, and a sequence has the same
+ * bytes alone or in any batch.
+ * batch == 0 is a no-op.  A row with no visible key (a sequence shorter than
+ * q_len, flagged MEMRA_DEVERR_BAD_SEQ_LEN, or of length 0) yields zeros. */
 int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
                       int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
                       int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,

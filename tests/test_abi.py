@@ -105,8 +105,10 @@ def test_host_validation_without_gpu(memra):
     assert _decode(memra, c, q=4097) == 1
     assert _decode(memra, c, scale=float("nan")) == 1
     assert _decode(memra, c, Q=0) == 1
-    assert _decode(memra, c, Q=9, Hq=16) == 2                           # 72 rows per KV head
-    assert _decode(memra, _cache(memra, head_dim=256), D=256, Q=5, Hq=16) == 2   # 40 rows at D 256
+    assert _decode(memra, c, Q=9, Hq=16, wsb=10) == 3                   # 72 rows per KV head pass the limits
+    assert _decode(memra, c, Q=17, Hq=16) == 2                          # q_len above MEMRA_MAX_Q_LEN
+    assert _decode(memra, c, Hq=258) == 2                               # group 129 > MEMRA_MAX_GROUP
+    assert _decode(memra, c, B=65536) == 2                              # grid z limit
     assert L.memra_read_status(None, None, None) == 1
     assert memra.status_string(3) == "workspace too small"
     assert memra.status_string(99) == "unknown status"

@@ -5,6 +5,8 @@ max |gpu - oracle| <= 2e-3 (fp16 output of fp32-accumulated attention, see
 the tolerance derivation in the design doc).  The pools start as seeded random
 bytes, so slots that were never written hold garbage the kernels must ignore.
 """
+from types import SimpleNamespace
+
 import numpy as np
 import pytest
 
@@ -450,3 +452,62 @@ def test_fused_step_bad_page_and_validation():
         memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, 1, dw.out, dw.workspace,
                           w.sm_scale)
     assert e.value.status == 1
+
+
+# --------------------------------------------- one numeric class (verify) ---
+# A verify row (q_len = K + 1, draft tokens K = 1..8) must carry the same bytes
+# as a plain q_len = 1 decode at that position over the same cache: the memra
+# README's speculative decode gated byte-identical to plain decode.
+
+def _decode_at_positions(dw, w):
+    """Plain q_len = 1 decode of every verify position; returns fp16 [B, Q, Hq, D]."""
+    import decode_attention_block_memra_gb300 as memra
+    B, Q = w.batch, w.q_len
+    outs = []
+    for qi in range(Q):
+        q1 = dw.q[:, qi:qi + 1].contiguous()
+        sl = (dw.seq_lens - (Q - 1 - qi)).to(torch.int32).contiguous()
+        o1 = torch.empty_like(q1)
+        memra.decode_attn(dw.cache, q1, dw.page_table, sl, w.max_seq_len, o1, dw.workspace, w.sm_scale)
+        outs.append(o1)
+    assert memra.read_status(dw.cache) == 0
+    return torch.cat(outs, dim=1).cpu().numpy()
+
+
+def _verify_vs_decode(w, fused):
+    from decode_attention_block_memra_gb300.runner import upload
+    import decode_attention_block_memra_gb300 as memra
+    dw = upload(w, fill_seed=2)
+    dw.step(fused=fused)
+    assert memra.read_status(dw.cache) == 0
+    verify = dw.out.cpu().numpy()
+    plain = _decode_at_positions(dw, w)
+    diff = np.argwhere(verify.view(np.uint16) != plain.view(np.uint16))
+    assert diff.size == 0, f"{len(diff)} elements differ, first (b, qi, head, j) {diff[:4].tolist()}"
+    return verify
+
+
+@pytest.mark.parametrize("K", range(1, 9))
+def test_verify_rows_equal_plain_decode(K):
+    Q = K + 1
+    # contexts: ragged, crossing the 1,024-token split boundary inside the
+    # verify window, one split, and a sequence made only of new tokens
+    seq_lens = [2051 + K, 1024 + Q // 2, 300 + K, Q]
+    w = W.make_workload(f"verify_k{K}", batch=4, q_len=Q, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=40 + K, seq_lens=seq_lens, permute_pages=True, extra_pages=2)
+    out = _verify_vs_decode(w, fused=(K % 2 == 0))
+    ref = attention.reference(w, rows=_sample_rows(w, 24, K))
+    assert_out_close(w, SimpleNamespace(out=out), ref)
+
+
+@pytest.mark.parametrize("K,D,kf,vf", [(3, 128, "q8_0", "q5_1"), (8, 128, "fp8", "q4_0"), (5, 256, "q8_0", "fp8")])
+def test_verify_rows_equal_plain_decode_across_split_size_step(K, D, kf, vf):
+    """The split size C(T) grows by 16 tokens inside the verify window: each row still matches its own decode."""
+    Q = K + 1
+    n_kv_heads = 32
+    S = max(1, torch.cuda.get_device_properties(0).multi_processor_count * 2 // n_kv_heads)
+    t_step = S * 16 * 64 + 1              # first length whose ceil(T / S) passes 1,024 (C: 1,024 -> 1,040)
+    seq_lens = [t_step + Q // 2, t_step + Q - 1]
+    w = W.make_workload("verify_cstep", batch=2, q_len=Q, n_heads=n_kv_heads, n_kv_heads=n_kv_heads, head_dim=D,
+                        k_fmt=kf, v_fmt=vf, seed=90 + K, seq_lens=seq_lens)
+    _verify_vs_decode(w, fused=True)
