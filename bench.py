@@ -37,7 +37,9 @@ BYTES_PER_TOKEN_HEAD = {  # per token per KV head, K + V, by head_dim (quantized
     ("fp8", "q5_1"): 224 / 128, ("fp8", "q4_0"): 200 / 128, ("fp8", "fp8"): 256 / 128,
 }
 KERNEL_SOURCES = ["decode_attention_block_memra_gb300/csrc/decode_kernel.cuh",
-                  "decode_attention_block_memra_gb300/csrc/memra_device.cuh", "include/memra.h"]
+                  "decode_attention_block_memra_gb300/csrc/memra_device.cuh",
+                  "decode_attention_block_memra_gb300/csrc/kv_quant.cuh",
+                  "decode_attention_block_memra_gb300/csrc/api.cu", "include/memra.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
