@@ -18,11 +18,19 @@ all in float64.  Rows with no visible key return zeros.  The shared-prefix
 workload needs nothing special here: page tables that point at the same pages
 read the same rows.
 
+Sliding window (the README's SWA ring, "Recent fixes" list): with a window of
+W tokens the row at position p sees only keys max(0, p - W + 1) .. p.  Ring
+page tables map position p to column (p // 16) % R of the sequence's row, so
+only the last R pages of a sequence hold rows.
+
 Pins: explicit triple loops on tiny inputs; a context of one token returns
 that V^ row; q = 0 returns the mean of the visible V^ rows; float64
 ``torch.nn.functional.scaled_dot_product_attention`` (a library routine) on
 the dequantized, GQA-expanded tensors with a causal mask; invariance under a
-permutation of the page pool (tests/test_oracle_attention.py).
+permutation of the page pool; for the window: explicit loops, a window of
+one returns the row's own V^, q = 0 returns the mean of the window, a window
+wider than the context is full attention, and float64 SDPA with a band mask
+(tests/test_oracle_attention.py).
 """
 from __future__ import annotations
 
@@ -33,8 +41,13 @@ from . import quant
 PAGE = 16
 
 
-def attention_rows(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, sm_scale: float) -> np.ndarray:
-    """q [Q, Hq, D], k_hat / v_hat [T, Hkv, D] -> out [Q, Hq, D] float64 (causal over the last Q keys)."""
+def attention_rows(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, sm_scale: float, window: int = 0,
+                   start: int = 0) -> np.ndarray:
+    """q [Q, Hq, D], k_hat / v_hat [T', Hkv, D] -> out [Q, Hq, D] float64 (causal over the last Q keys).
+
+    The rows hold positions start .. start + T' - 1 of the sequence.  window > 0
+    hides keys more than window - 1 positions before the query row.
+    """
     q = np.asarray(q, dtype=np.float64)
     k_hat = np.asarray(k_hat, dtype=np.float64)
     v_hat = np.asarray(v_hat, dtype=np.float64)
@@ -46,12 +59,18 @@ def attention_rows(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, sm_scale
         kh = h // G
         s_all = k_hat[:, kh, :] @ q[:, h, :].T * sm_scale          # [T, Q]
         for i in range(Q):
-            last = T - Q + i                                       # last visible key
+            last = T - Q + i                                       # last visible key (row index)
             if last < 0:
                 continue
-            s = s_all[: last + 1, i]
+            first = 0
+            if window > 0:
+                first_pos = max(0, start + last - window + 1)
+                if first_pos < start:
+                    raise ValueError("the window reaches keys before the first row given")
+                first = first_pos - start
+            s = s_all[first: last + 1, i]
             p = np.exp(s - s.max())
-            out[i, h] = (p @ v_hat[: last + 1, kh, :]) / p.sum()
+            out[i, h] = (p @ v_hat[first: last + 1, kh, :]) / p.sum()
     return out
 
 
@@ -64,11 +83,19 @@ def quantize_cache(w) -> dict:
     return out
 
 
+def first_position(w, b: int) -> int:
+    """First position of sequence b that holds a row (0 unless the page table is a ring)."""
+    return int(w.first_pos[b]) if getattr(w, "ring", False) else 0
+
+
 def sequence_rows(w, b: int) -> np.ndarray:
-    """Indices (into the unique rows) of sequence b's tokens 0..T_b-1, through its page table."""
+    """Indices (into the unique rows) of sequence b's tokens first_position .. T_b - 1, through its page table."""
     T = int(w.seq_lens[b])
-    tok = np.arange(T, dtype=np.int64)
-    slots = w.page_table[b, tok // PAGE].astype(np.int64) * PAGE + tok % PAGE
+    tok = np.arange(first_position(w, b), T, dtype=np.int64)
+    col = tok // PAGE
+    if getattr(w, "ring", False):
+        col = col % w.page_table.shape[1]
+    slots = w.page_table[b, col].astype(np.int64) * PAGE + tok % PAGE
     order = np.argsort(w.slots, kind="stable")
     pos = np.searchsorted(w.slots[order], slots)
     rows = order[pos]
@@ -102,7 +129,8 @@ def reference(w, cache=None, rows=None) -> np.ndarray:
             k_hat = quant.dequantize_rows(quant.select_rows(cache["k"][kh], r))[:, None, :]
             v_hat = quant.dequantize_rows(quant.select_rows(cache["v"][kh], r))[:, None, :]
             heads = slice(kh * G, (kh + 1) * G)
-            out[b, :, heads, :] = attention_rows(w.q[b, :, heads, :], k_hat, v_hat, w.sm_scale)
+            out[b, :, heads, :] = attention_rows(w.q[b, :, heads, :], k_hat, v_hat, w.sm_scale,
+                                                 window=getattr(w, "window", 0), start=first_position(w, b))
     if rows is not None:
         mask = np.zeros(out.shape[:3], dtype=bool)
         for (b, i, h) in rows:

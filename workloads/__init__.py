@@ -23,6 +23,10 @@ format names).  The pages name no random generator, so the recipe is:
 * The last ``q_len`` rows of every sequence are the rows the step appends
   (quantize-append runs inside the timed step); all other rows are written
   into the cache before timing.
+* Sliding-window workloads (the README's SWA ring, "Recent fixes"): every
+  sequence owns a ring of R pages and position p lives in ring page
+  (p // 16) % R, so only the rows of the last R pages exist; they are drawn
+  sequence-major in position order (q -> k -> v -> page permutation).
 """
 from __future__ import annotations
 
@@ -58,6 +62,9 @@ class Workload:
     k_scale: float = 1.0          # fp8 only: float32 per-tensor scale of K
     v_scale: float = 1.0          # fp8 only: float32 per-tensor scale of V
     shared_prefix: int = 0
+    window: int = 0               # sliding window in tokens (0: every earlier key is visible)
+    ring: bool = False            # page_table rows are rings: position p -> column (p // 16) % columns
+    first_pos: np.ndarray | None = None   # int64 [B] first position with a row (ring workloads)
     notes: dict = field(default_factory=dict)
 
     @property
@@ -188,6 +195,48 @@ def make_workload(name: str, *, batch: int, q_len: int, n_heads: int, n_kv_heads
                  head_dim=head_dim, k_fmt=k_fmt, v_fmt=v_fmt, seq_lens=seq_lens.astype(np.int32),
                  page_table=page_table, num_pages=num_pages, q=q, slots=slots, k_rows=k_rows, v_rows=v_rows,
                  step_rows=step_rows.astype(np.int64), shared_prefix=shared_prefix)
+    w.k_scale, w.v_scale = _fp8_scales(w)
+    return w
+
+
+def min_ring_pages(window: int, q_len: int) -> int:
+    """Fewest ring pages that hold every key a window of `window` tokens shows to q_len query rows."""
+    return (window + q_len - 2) // PAGE_SIZE + 2
+
+
+def make_window_workload(name: str, *, batch: int, q_len: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                         k_fmt: str, v_fmt: str, seed: int, seq_lens, window: int, ring_pages: int | None = None,
+                         permute_pages: bool = False, extra_pages: int = 0) -> Workload:
+    """Sliding-window attention over a ring of pages per sequence."""
+    assert k_fmt in K_FORMATS and v_fmt in V_FORMATS and window >= 1
+    R = min_ring_pages(window, q_len) if ring_pages is None else int(ring_pages)
+    assert R >= min_ring_pages(window, q_len)
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64).reshape(batch)
+    assert (seq_lens >= max(q_len, 1)).all()
+    first = np.maximum(0, ((seq_lens - 1) // PAGE_SIZE - R + 1) * PAGE_SIZE)
+    counts = seq_lens - first
+    n_unique = int(counts.sum())
+    q = _normal_f16(rng, (batch, q_len, n_heads, head_dim))
+    k_rows = _normal_f16(rng, (n_unique, n_kv_heads, head_dim))
+    v_rows = _normal_f16(rng, (n_unique, n_kv_heads, head_dim))
+    num_pages = batch * R + extra_pages
+    phys = rng.permutation(num_pages).astype(np.int64) if permute_pages else np.arange(num_pages, dtype=np.int64)
+    page_table = phys[:batch * R].reshape(batch, R).astype(np.int32)
+    slots, step = [], []
+    base = 0
+    for b in range(batch):
+        pos = np.arange(first[b], seq_lens[b], dtype=np.int64)
+        slots.append(page_table[b, (pos // PAGE_SIZE) % R].astype(np.int64) * PAGE_SIZE + pos % PAGE_SIZE)
+        step.append(np.arange(base + counts[b] - q_len, base + counts[b], dtype=np.int64))
+        base += int(counts[b])
+    w = Workload(name=name, batch=batch, q_len=q_len, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                 head_dim=head_dim, k_fmt=k_fmt, v_fmt=v_fmt, seq_lens=seq_lens.astype(np.int32),
+                 page_table=page_table, num_pages=num_pages, q=q,
+                 slots=np.concatenate(slots).astype(np.int32) if batch else np.zeros(0, np.int32),
+                 k_rows=k_rows, v_rows=v_rows,
+                 step_rows=np.concatenate(step) if batch else np.zeros(0, np.int64),
+                 window=int(window), ring=True, first_pos=first.astype(np.int64))
     w.k_scale, w.v_scale = _fp8_scales(w)
     return w
 
