@@ -73,6 +73,14 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
                           [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                   ctypes.c_void_p]),
+    "memra_decode_attn_window": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
+                                 [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                  ctypes.c_void_p]),
+    "memra_decode_step_window": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
+                                 [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
+                                                         ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "memra_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
                                                  ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
                                   [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
@@ -190,10 +198,17 @@ def _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm
 
 
 def decode_attn(cache: KVCache, q, page_table, seq_lens, max_seq_len: int, out, workspace, sm_scale=None,
-                stream=None) -> None:
-    """memra_decode_attn: q fp16 [B, Q, Hq, D] -> out fp16 [B, Q, Hq, D]."""
-    _check(lib().memra_decode_attn(*_decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace,
-                                                 sm_scale), _stream(stream)), "memra_decode_attn")
+                stream=None, window: int = 0) -> None:
+    """memra_decode_attn: q fp16 [B, Q, Hq, D] -> out fp16 [B, Q, Hq, D].
+
+    window > 0: memra_decode_attn_window (sliding window; page_table rows are rings).
+    """
+    a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
+    if window:
+        _check(lib().memra_decode_attn_window(*a[:12], int(window), *a[12:], _stream(stream)),
+               "memra_decode_attn_window")
+        return
+    _check(lib().memra_decode_attn(*a, _stream(stream)), "memra_decode_attn")
 
 
 def decode_attn_partials(cache: KVCache, q, page_table, seq_lens, max_seq_len: int, out, workspace, sm_scale=None,
@@ -211,13 +226,18 @@ def decode_attn_combine(cache: KVCache, seq_lens, max_seq_len: int, max_pages_pe
 
 
 def decode_step(cache: KVCache, k_new, v_new, q, page_table, seq_lens, max_seq_len: int, out, workspace,
-                sm_scale=None, stream=None) -> None:
+                sm_scale=None, stream=None, window: int = 0) -> None:
     """memra_decode_step: store the step's rows (k_new, v_new fp16 [B, Q, Hkv, D]) and attend, in one pass.
 
     seq_lens include the Q new tokens; their rows go to the positions
-    seq_lens[b] - Q .. seq_lens[b] - 1 of each sequence's pages.
+    seq_lens[b] - Q .. seq_lens[b] - 1 of each sequence's pages.  window > 0:
+    memra_decode_step_window (sliding window; page_table rows are rings).
     """
     a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
+    if window:
+        _check(lib().memra_decode_step_window(a[0], _ptr(k_new), _ptr(v_new), *a[1:12], int(window), *a[12:],
+                                              _stream(stream)), "memra_decode_step_window")
+        return
     _check(lib().memra_decode_step(a[0], _ptr(k_new), _ptr(v_new), *a[1:], _stream(stream)), "memra_decode_step")
 
 

@@ -117,7 +117,14 @@ struct DecodeArgs {
   void *workspace;
   size_t workspace_bytes;
   void *out;
+  int32_t window;     // sliding window (tokens); > 0 also makes page_table rows rings
 };
+
+// Longest key range any position of the call can have: the window (+ the part
+// of its first page before it) or the whole context.
+int64_t longest_range(int32_t max_seq_len, int32_t window) {
+  return window > 0 ? std::min<int64_t>(max_seq_len, static_cast<int64_t>(window) + kPage - 1) : max_seq_len;
+}
 
 int check_decode(const DecodeArgs &a) {
   int st = check_cache(a.cache);
@@ -136,6 +143,10 @@ int check_decode(const DecodeArgs &a) {
       (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
     return MEMRA_ERR_INVALID_ARG;
   if (a.max_pages_per_seq < 1) return MEMRA_ERR_INVALID_ARG;
+  if (a.window < 0) return MEMRA_ERR_INVALID_ARG;
+  // a ring must hold every page that the window of any query row reaches
+  if (a.window > 0 && a.max_pages_per_seq < (static_cast<int64_t>(a.window) + a.q_len - 2) / kPage + 2)
+    return MEMRA_ERR_INVALID_ARG;
   const size_t need = workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, nullptr);
   if (a.workspace_bytes < need) return MEMRA_ERR_WORKSPACE;
   if (need > 0 && (!a.workspace || !aligned16(a.workspace))) return MEMRA_ERR_INVALID_ARG;
@@ -171,6 +182,8 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.q_len = a.q_len;
   p.n_heads = a.n_heads;
   p.group = group;
+  p.window = a.window;
+  p.ring = a.window > 0 ? 1 : 0;
   p.ngh = pl.ngh;
   p.ngh_q = pl.ngh_q;
   p.nsplit_max = pl.nsplit_max;
@@ -180,9 +193,10 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
   p.k_scale = c.k_scale;
-  // no sequence has more splits than min(ceil(T/1024), max(target, ceil(T/8192)))
-  const int64_t most = std::min<int64_t>(pl.nsplit_max, std::max<int64_t>(p.split_target,
-                                                                          ceil_div(a.max_seq_len, kSplitTokensMax)));
+  // no position has more splits than min(ceil(L/1024), max(target, ceil(L/8192))), L its key range
+  const int64_t L = longest_range(a.max_seq_len, a.window);
+  const int64_t most = std::min<int64_t>(ceil_div(L, kSplitTokens),
+                                         std::max<int64_t>(p.split_target, ceil_div(L, kSplitTokensMax)));
   // x: split-major, then query position and head group (the CTAs that read
   // the same pages run side by side and share them through L2)
   const dim3 grid(static_cast<unsigned>(most * pl.ngh_q), static_cast<unsigned>(c.n_kv_heads),
@@ -193,8 +207,8 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
 }
 
 int run_combine(const memra_kv_cache *c, const int32_t *seq_lens, int32_t max_seq_len, int32_t max_pages,
-                int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, const void *workspace, void *out,
-                cudaStream_t st) {
+                int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, int32_t window,
+                const void *workspace, void *out, cudaStream_t st) {
   size_t lse_off = 0;
   workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len, &lse_off);
   CombineParams p;
@@ -209,6 +223,8 @@ int run_combine(const memra_kv_cache *c, const int32_t *seq_lens, int32_t max_se
   p.max_seq_len = max_seq_len;
   p.max_pages = max_pages;
   p.nsplit_max = static_cast<int>(ceil_div(max_seq_len, kSplitTokens));
+  p.window = window;
+  p.ring = window > 0 ? 1 : 0;
   Plan pl;
   int rc = make_plan(head_dim, c->k_fmt, c->v_fmt, q_len, n_heads / c->n_kv_heads, max_seq_len, &pl);
   if (rc) return rc;
@@ -256,7 +272,7 @@ int memra_decode_attn_partials(const memra_kv_cache *cache, const void *q, const
                                int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
                                void *workspace, size_t workspace_bytes, void *out, void *stream) {
   DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
-               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
+               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0};
   int st = check_decode(a);
   if (st || batch == 0) return st;
   return run_partials(a, nullptr, nullptr, static_cast<cudaStream_t>(stream));
@@ -276,23 +292,40 @@ int memra_decode_attn_combine(const memra_kv_cache *cache, const int32_t *seq_le
   const size_t need = workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len, nullptr);
   if (workspace_bytes < need) return MEMRA_ERR_WORKSPACE;
   if (need > 0 && (!workspace || !aligned16(workspace))) return MEMRA_ERR_INVALID_ARG;
-  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
+  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, 0, workspace,
                      out, static_cast<cudaStream_t>(stream));
 }
+
+}  // extern "C"
+
+namespace {
+
+// Split pass (with the fused append when k_new / v_new are given), then the combine.
+int decode_both_passes(const DecodeArgs &a, const void *k_new, const void *v_new, void *stream) {
+  int st = check_decode(a);
+  if (st || a.batch == 0) return st;
+  if (k_new || v_new) {
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return MEMRA_ERR_INVALID_ARG;
+    if (a.max_seq_len < a.q_len) return MEMRA_ERR_INVALID_ARG;     // no sequence can hold the new rows
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_partials(a, k_new, v_new, s);
+  if (st) return st;
+  return run_combine(a.cache, a.seq_lens, a.max_seq_len, a.max_pages_per_seq, a.batch, a.q_len, a.n_heads,
+                     a.head_dim, a.window, a.workspace, a.out, s);
+}
+
+}  // namespace
+
+extern "C" {
 
 int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
                       int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
                       int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
                       void *workspace, size_t workspace_bytes, void *out, void *stream) {
-  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
-               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
-  int st = check_decode(a);
-  if (st || batch == 0) return st;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_partials(a, nullptr, nullptr, s);
-  if (st) return st;
-  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
-                     out, s);
+  const DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0};
+  return decode_both_passes(a, nullptr, nullptr, stream);
 }
 
 int memra_decode_step(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
@@ -300,17 +333,31 @@ int memra_decode_step(const memra_kv_cache *cache, const void *k_new, const void
                       int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
                       int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
                       void *stream) {
-  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
-               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out};
-  int st = check_decode(a);
-  if (st || batch == 0) return st;
-  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return MEMRA_ERR_INVALID_ARG;
-  if (max_seq_len < q_len) return MEMRA_ERR_INVALID_ARG;     // no sequence can hold the new rows
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_partials(a, k_new, v_new, s);
-  if (st) return st;
-  return run_combine(cache, seq_lens, max_seq_len, max_pages_per_seq, batch, q_len, n_heads, head_dim, workspace,
-                     out, s);
+  if (!k_new || !v_new) return MEMRA_ERR_INVALID_ARG;
+  const DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0};
+  return decode_both_passes(a, k_new, v_new, stream);
+}
+
+int memra_decode_attn_window(const memra_kv_cache *cache, const void *q, const int32_t *ring_table,
+                             int32_t ring_pages, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                             int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
+                             int32_t window, void *workspace, size_t workspace_bytes, void *out, void *stream) {
+  if (window < 1) return MEMRA_ERR_INVALID_ARG;
+  const DecodeArgs a{cache, q, ring_table, ring_pages, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, window};
+  return decode_both_passes(a, nullptr, nullptr, stream);
+}
+
+int memra_decode_step_window(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                             const int32_t *ring_table, int32_t ring_pages, const int32_t *seq_lens,
+                             int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                             int32_t head_dim, float sm_scale, int32_t window, void *workspace,
+                             size_t workspace_bytes, void *out, void *stream) {
+  if (window < 1 || !k_new || !v_new) return MEMRA_ERR_INVALID_ARG;
+  const DecodeArgs a{cache, q, ring_table, ring_pages, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, window};
+  return decode_both_passes(a, k_new, v_new, stream);
 }
 
 int memra_read_status(const memra_kv_cache *cache, int32_t *flags, void *stream) {

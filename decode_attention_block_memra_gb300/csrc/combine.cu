@@ -31,15 +31,13 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
   const int b = row / (p.q_len * p.n_heads);
   const int qi = (row / p.n_heads) % p.q_len;
   // keys visible to this row's position (its own split plan, as in the split kernel)
-  const int T = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status, false) - p.q_len +
-                qi + 1;
+  const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.ring, p.status, false);
+  const int ns = key_range(Tseq, p.q_len, qi, p.window, p.split_target).ns;
   __half *dst = p.out + static_cast<size_t>(row) * D;
-  if (T <= 0) {                                     // no visible key: zeros
+  if (ns == 0) {                                    // no visible key: zeros
     for (int j = threadIdx.x; j < D; j += blockDim.x) dst[j] = __float2half(0.f);
     return;
   }
-  const int C = split_tokens(T, p.split_target);
-  const int ns = (T + C - 1) / C;
   if (ns == 1) return;                              // the split kernel wrote this row
   const float *lse = p.lse_part + static_cast<size_t>(row) * p.nsplit_max;
   const float *op = p.o_part + static_cast<size_t>(row) * p.nsplit_max * D + lane * PER;

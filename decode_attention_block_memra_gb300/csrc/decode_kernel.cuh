@@ -70,6 +70,8 @@ struct DecodeParams {
   const __half *k_new;
   const __half *v_new;
   int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group;
+  int window;         // sliding window in tokens, 0 = none
+  int ring;           // 1: page_table rows are rings of max_pages columns (position p -> (p / 16) % max_pages)
   int ngh;            // groups of 8 query heads per KV head: ceil(group / 8)
   int ngh_q;          // CTAs per (split, KV head, sequence): q_len * ngh
   int nsplit_max, num_stages, split_target;
@@ -83,6 +85,7 @@ struct CombineParams {
   __half *out;
   int32_t *status;
   int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max, split_target;
+  int window, ring;
 };
 
 cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
@@ -105,13 +108,36 @@ struct MergeLayout {
   static constexpr int kBytes = (kO + 2 * kM + kTerm) * 4;
 };
 
-// Context length after the same clamping the combine kernel applies.
-__device__ __forceinline__ int clamp_seq_len(int T, int q_len, int max_seq_len, int max_pages, int32_t *status,
-                                             bool report) {
-  int Tc = min(T, min(max_seq_len, max_pages * kPage));
+// Context length after the same clamping the combine kernel applies.  A
+// linear page table bounds it by its columns; a ring does not.
+__device__ __forceinline__ int clamp_seq_len(int T, int q_len, int max_seq_len, int max_pages, bool ring,
+                                             int32_t *status, bool report) {
+  int Tc = min(T, max_seq_len);
+  if (!ring) Tc = min(Tc, max_pages * kPage);
   Tc = max(Tc, 0);
   if (report && (Tc != T || T < q_len)) flag_error(status, MEMRA_DEVERR_BAD_SEQ_LEN);
   return Tc;
+}
+
+// The keys a query position sees and how they are split; the split kernel and
+// the combine derive it from the same numbers.
+struct KeyRange {
+  int T;      // one past the last visible key (the position + 1)
+  int lo;     // first visible key (window), 0 without one
+  int base;   // lo rounded down to its page: splits start here
+  int C;      // split size
+  int ns;     // splits
+};
+
+__device__ __forceinline__ KeyRange key_range(int Tseq, int q_len, int qi, int window, int split_target) {
+  KeyRange k;
+  k.T = Tseq - q_len + qi + 1;
+  k.lo = window > 0 ? max(0, k.T - window) : 0;
+  k.base = k.lo & ~(kPage - 1);
+  const int L = k.T - k.base;
+  k.C = split_tokens(L, split_target);
+  k.ns = k.T > 0 ? (L + k.C - 1) / k.C : 0;
+  return k;
 }
 
 template <int KF>
@@ -172,23 +198,23 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   const int vr = blockIdx.x % p.ngh_q, split = blockIdx.x / p.ngh_q;
   const int qi = vr / p.ngh, hg = vr % p.ngh;
   const int kvh = blockIdx.y, b = blockIdx.z;
-  const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.status,
+  const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.ring, p.status,
                                  blockIdx.x == 0 && kvh == 0 && tid == 0);
-  const int T = Tseq - p.q_len + qi + 1;
-  if (T <= 0) return;
-  const int C = split_tokens(T, p.split_target);
-  const int tok0 = split * C;
-  if (tok0 >= T) return;
+  const KeyRange kr = key_range(Tseq, p.q_len, qi, p.window, p.split_target);
+  const int T = kr.T, lo = kr.lo, C = kr.C;
+  if (T <= 0 || split >= kr.ns) return;
+  const int tok0 = kr.base + split * C;
   const int npages = (min(T, tok0 + C) - tok0 + kPage - 1) / kPage;
-  const int nsplit_b = (T + C - 1) / C;
+  const int nsplit_b = kr.ns;
   const int nrows = min(8, p.group - 8 * hg);   // query heads of this CTA
   const int R = kWarps;                         // page lanes: warp r takes pages r, r + R, ...
   const int r = warp;
 
   {
-    const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages + tok0 / kPage;
+    const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
     for (int i = tid; i < npages; i += kThreads) {
-      const int pid = pt[i];
+      const int j = tok0 / kPage + i;                 // logical page of the sequence
+      const int pid = pt[p.ring ? j % p.max_pages : j];
       const bool ok = pid >= 0 && pid < p.num_pages;
       if (!ok) flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
       pid_s[i] = ok ? pid : -1;
@@ -357,7 +383,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       // Pages wholly inside every row's visible range (all but the last one or
       // two of a sequence) take a path without any masking code.
       const int pos_first = tok0 + i * kPage;
-      const bool plain = pos_first + kPage <= T;
+      const bool plain = pos_first >= lo && pos_first + kPage <= T;
       auto page = [&](auto tail) {
         const uint32_t ka = ring + s * STAGE;
         const uint32_t va = ka + KSEG;
@@ -448,10 +474,11 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
             for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
           if (masked) {
             const int t0 = pos0 + g, t1 = pos0 + g + 8;
-            s4[n][0] = t0 < T ? s4[n][0] : -INFINITY;
-            s4[n][1] = t0 < T ? s4[n][1] : -INFINITY;
-            s4[n][2] = t1 < T ? s4[n][2] : -INFINITY;
-            s4[n][3] = t1 < T ? s4[n][3] : -INFINITY;
+            const bool v0 = t0 < T && t0 >= lo, v1 = t1 < T && t1 >= lo;
+            s4[n][0] = v0 ? s4[n][0] : -INFINITY;
+            s4[n][1] = v0 ? s4[n][1] : -INFINITY;
+            s4[n][2] = v1 ? s4[n][2] : -INFINITY;
+            s4[n][3] = v1 ? s4[n][3] : -INFINITY;
           }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -504,8 +531,9 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
         uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
         if (partial) {
           const int t = pos0 + 2 * c;
-          m01 = (t < T ? 0x0000FFFFu : 0u) | (t + 1 < T ? 0xFFFF0000u : 0u);
-          m89 = (t + 8 < T ? 0x0000FFFFu : 0u) | (t + 9 < T ? 0xFFFF0000u : 0u);
+          auto vis = [&](int u) { return u < T && u >= lo; };
+          m01 = (vis(t) ? 0x0000FFFFu : 0u) | (vis(t + 1) ? 0xFFFF0000u : 0u);
+          m89 = (vis(t + 8) ? 0x0000FFFFu : 0u) | (vis(t + 9) ? 0xFFFF0000u : 0u);
         }
         if constexpr (kVq) {
           constexpr int DOFF = kQ5 ? 10 * D : 8 * D;

@@ -34,15 +34,16 @@ class DeviceWorkload:
         of memra_kv_append followed by memra_decode_attn.
         """
         w = self.w
+        window = getattr(w, "window", 0)
         if fused:
             B, Q = w.batch, w.q_len
             decode_step(self.cache, self.step_k.view(B, Q, w.n_kv_heads, w.head_dim),
                         self.step_v.view(B, Q, w.n_kv_heads, w.head_dim), self.q, self.page_table, self.seq_lens,
-                        w.max_seq_len, self.out, self.workspace, w.sm_scale, stream=stream)
+                        w.max_seq_len, self.out, self.workspace, w.sm_scale, stream=stream, window=window)
             return
         kv_append(self.cache, self.step_k, self.step_v, self.step_slots, stream=stream)
         decode_attn(self.cache, self.q, self.page_table, self.seq_lens, w.max_seq_len, self.out, self.workspace,
-                    w.sm_scale, stream=stream)
+                    w.sm_scale, stream=stream, window=window)
 
 
 def upload(w, fill_seed: int | None = None, device="cuda", prefill_chunk: int = 1 << 20) -> DeviceWorkload:

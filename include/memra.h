@@ -221,6 +221,30 @@ int memra_decode_step(const memra_kv_cache *cache, const void *k_new, const void
                       int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
                       void *stream);
 
+/* Sliding-window attention over ring page tables (the memra README's opt-in
+ * SWA ring in its "Recent fixes" list, which right-sizes the KV of sliding-
+ * window layers: only the last pages of a sequence are kept, reused modulo
+ * the ring).  Same arguments and results as memra_decode_attn /
+ * memra_decode_step, except:
+ *   ring_table   device int32 [batch][ring_pages]: position p of sequence b
+ *                lives in page ring_table[b][(p / 16) % ring_pages], slot p % 16
+ *                (memra_kv_append takes those slots)
+ *   ring_pages   >= (window + q_len - 2) / 16 + 2, so that the ring holds every
+ *                key any query row sees; else MEMRA_ERR_INVALID_ARG
+ *   window       >= 1: the row at position p sees keys max(0, p - window + 1) .. p
+ *   seq_lens     are not bounded by the ring (only by max_seq_len)
+ * The workspace is memra_decode_attn_workspace_bytes(...) of the same sizes.
+ * Verify rows stay byte-identical to q_len = 1 calls at their positions. */
+int memra_decode_attn_window(const memra_kv_cache *cache, const void *q, const int32_t *ring_table,
+                             int32_t ring_pages, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                             int32_t q_len, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float sm_scale,
+                             int32_t window, void *workspace, size_t workspace_bytes, void *out, void *stream);
+int memra_decode_step_window(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                             const int32_t *ring_table, int32_t ring_pages, const int32_t *seq_lens,
+                             int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                             int32_t head_dim, float sm_scale, int32_t window, void *workspace,
+                             size_t workspace_bytes, void *out, void *stream);
+
 /* Fixed size of the device array that memra_decode_attn_noalloc uses for the
  * split-K partials (held on every device that calls it, until exit). */
 #define MEMRA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -511,3 +511,83 @@ def test_verify_rows_equal_plain_decode_across_split_size_step(K, D, kf, vf):
     w = W.make_workload("verify_cstep", batch=2, q_len=Q, n_heads=n_kv_heads, n_kv_heads=n_kv_heads, head_dim=D,
                         k_fmt=kf, v_fmt=vf, seed=90 + K, seq_lens=seq_lens)
     _verify_vs_decode(w, fused=True)
+
+
+# ------------------------------------------- sliding window over ring pages --
+# memra_decode_attn_window / memra_decode_step_window: the row at position p
+# sees keys max(0, p - W + 1) .. p, and each sequence keeps only a ring of pages.
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kf,vf", FORMAT_PAIRS)
+def test_window_formats(kf, vf, D):
+    # contexts below, at and far past the window (the ring wraps several times), ragged, shuffled ring pages
+    w = W.make_window_workload("win_fmt", batch=4, q_len=1, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt=kf,
+                               v_fmt=vf, seed=300 + D + FORMAT_PAIRS.index((kf, vf)),
+                               seq_lens=[37, 300, 1111, 2900], window=300, permute_pages=True, extra_pages=3)
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("window,q_len,seq_lens", [
+    (1, 1, [1, 17, 500]),            # each row sees only itself
+    (16, 4, [16, 20, 333]),          # window of one page
+    (1000, 4, [999, 1000, 1001, 5000]),
+    (1500, 2, [4097, 2050]),         # splits of a window range (C = 1,024), window start mid-page
+    (4096, 8, [262144]),             # an SWA layer of a 262,144-token session: a 258-page ring
+])
+def test_window_shapes(window, q_len, seq_lens):
+    w = W.make_window_workload("win", batch=len(seq_lens), q_len=q_len, n_heads=32, n_kv_heads=4, head_dim=128,
+                               k_fmt="q8_0", v_fmt="q5_1", seed=window + q_len, seq_lens=seq_lens, window=window,
+                               permute_pages=True, extra_pages=2)
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+@pytest.mark.parametrize("K", [1, 3, 8])
+def test_window_verify_rows_equal_plain_decode(K):
+    Q = K + 1
+    w = W.make_window_workload(f"win_verify{K}", batch=3, q_len=Q, n_heads=32, n_kv_heads=4, head_dim=128,
+                               k_fmt="q8_0", v_fmt="q5_1", seed=70 + K, seq_lens=[3000 + K, 1030, Q], window=1025,
+                               permute_pages=True)
+    from decode_attention_block_memra_gb300.runner import upload
+    import decode_attention_block_memra_gb300 as memra
+    dw = upload(w, fill_seed=3)
+    dw.step(fused=True)
+    assert memra.read_status(dw.cache) == 0
+    verify = dw.out.cpu().numpy()
+    for qi in range(Q):
+        q1 = dw.q[:, qi:qi + 1].contiguous()
+        sl = (dw.seq_lens - (Q - 1 - qi)).to(torch.int32).contiguous()
+        o1 = torch.empty_like(q1)
+        memra.decode_attn(dw.cache, q1, dw.page_table, sl, w.max_seq_len, o1, dw.workspace, w.sm_scale,
+                          window=w.window)
+        assert np.array_equal(o1.cpu().numpy()[:, 0].view(np.uint16), verify[:, qi].view(np.uint16)), qi
+    assert memra.read_status(dw.cache) == 0
+    assert_out_close(w, SimpleNamespace(out=verify), attention.reference(w))
+
+
+def test_window_fused_step_matches_two_calls():
+    w = W.make_window_workload("win_fused", batch=3, q_len=4, n_heads=16, n_kv_heads=2, head_dim=128,
+                               k_fmt="q8_0", v_fmt="q5_1", seed=123, seq_lens=[5000, 700, 4], window=700,
+                               permute_pages=True, extra_pages=1)
+    assert_fused_matches(w)
+
+
+def test_window_validation():
+    import decode_attention_block_memra_gb300 as memra
+    w = W.make_window_workload("win_val", batch=1, q_len=2, n_heads=8, n_kv_heads=2, head_dim=128, k_fmt="q8_0",
+                               v_fmt="q5_1", seed=5, seq_lens=[100], window=40)
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w)
+    with pytest.raises(memra.MemraError) as e:           # the ring cannot hold a 100-token window
+        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
+                          w.sm_scale, window=100)
+    assert e.value.status == 1
+    with pytest.raises(memra.MemraError) as e:           # negative window
+        memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
+                          w.sm_scale, window=-3)
+    assert e.value.status == 1
