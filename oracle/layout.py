@@ -27,8 +27,20 @@ V side
     q4_0 d      8 D + ((c nb + b) 4 + 2 p + f) 2
     fp8 byte    (b 32 + lane) 16 + 8 h + 2 (2 p + s) + f
 
-Segment sizes: K q8_0 17 D, K fp8 16 D, V q5_1 12 D, V q4_0 9 D, V fp8 16 D.
-Every byte of a segment belongs to exactly one token.
+NVFP4 (K or V; 16-element blocks, b16 = j // 16, r = j % 16; each 32-bit word
+of a lane holds the 8 codes of one m16n8k16 A fragment, 4 bits each, and every
+byte two codes of one token)
+    K codes     lane = 4 (t % 8) + (r % 8) // 2
+                byte ((b16 // 4) 32 + lane) 16 + (b16 % 4) 4 + (t // 8) + 2 (r // 8),
+                bits 4 (r % 2) ..                          (elements r, r + 1 share a byte)
+    K scales    8 D + t (D/16) + b16                       (e4m3 bytes)
+    V codes     c = (t % 8) // 2, lane = 4 (r % 8) + c
+                byte ((b16 // 4) 32 + lane) 16 + (b16 % 4) 4 + (t % 2) + 2 (t // 8),
+                bits 4 (r // 8) ..                         (elements r, r + 8 share a byte)
+    V scales    8 D + (c (D/16) + b16) 4 + (t % 2) + 2 (t // 8)
+
+Segment sizes: K q8_0 17 D, K fp8 16 D, K nvfp4 9 D, V q5_1 12 D, V q4_0 9 D,
+V fp8 16 D, V nvfp4 9 D.  Every byte of a segment belongs to exactly one token.
 
 Pin: this module has no source outside the library's own header, so its
 parity is pinned only by (a) the round trip unpack(pack(x)) == x, (b) the
@@ -43,11 +55,11 @@ PAGE = 16
 
 
 def k_segment_bytes(fmt: str, D: int) -> int:
-    return {"q8_0": 17 * D, "fp8": 16 * D}[fmt]
+    return {"q8_0": 17 * D, "fp8": 16 * D, "nvfp4": 9 * D}[fmt]
 
 
 def v_segment_bytes(fmt: str, D: int) -> int:
-    return {"q5_1": 12 * D, "q4_0": 9 * D, "fp8": 16 * D}[fmt]
+    return {"q5_1": 12 * D, "q4_0": 9 * D, "fp8": 16 * D, "nvfp4": 9 * D}[fmt]
 
 
 def segment_bytes(side: str, fmt: str, D: int) -> int:
@@ -105,6 +117,29 @@ def v_fp8_offset(t, j, D):
     return (b * 32 + lane) * 16 + 8 * h + 2 * (2 * p + s) + f
 
 
+# ------------------------------------------------------------ NVFP4 side ---
+
+def nvfp4_code_offset(side: str, t, j, D):
+    """(byte, shift) of the E2M1 code of element j of token t."""
+    b16, r = j // 16, j % 16
+    if side == "k":
+        lane = 4 * (t % 8) + (r % 8) // 2
+        byte_in_word = t // 8 + 2 * (r // 8)
+        shift = 4 * (r % 2)
+    else:
+        lane = 4 * (r % 8) + (t % 8) // 2
+        byte_in_word = t % 2 + 2 * (t // 8)
+        shift = 4 * (r // 8)
+    return ((b16 // 4) * 32 + lane) * 16 + (b16 % 4) * 4 + byte_in_word, shift
+
+
+def nvfp4_scale_offset(side: str, t, b16, D):
+    if side == "k":
+        return 8 * D + t * (D // 16) + b16
+    c = (t % 8) // 2
+    return 8 * D + (c * (D // 16) + b16) * 4 + t % 2 + 2 * (t // 8)
+
+
 # ------------------------------------------------- one token row -> bytes ---
 
 def _fp16_bytes(x: np.ndarray) -> np.ndarray:
@@ -127,6 +162,23 @@ def row_bytes(side: str, fields: dict, t: np.ndarray, D: int):
     nb = D // 32
     j = np.arange(D, dtype=np.int64).reshape(1, D)
     offs, vals = [], []
+    if fmt == "nvfp4":
+        # two codes of the row per byte: elements (j, j + 1) for K, (j, j + 8) for V
+        if side == "k":
+            lo_j = j[:, 0::2]
+            hi_q = q[:, 1::2]
+        else:
+            lo_j = j[:, (j[0] % 16) < 8]
+            hi_q = q[:, (j[0] % 16) >= 8]
+        off, sh = nvfp4_code_offset(side, t, lo_j, D)
+        assert (np.asarray(sh) == 0).all()
+        offs.append(np.broadcast_to(off, (N, D // 2)))
+        vals.append((q[:, lo_j[0]] | (hi_q << 4)).astype(np.uint8))
+        nb16 = D // 16
+        bb = np.arange(nb16, dtype=np.int64).reshape(1, nb16)
+        offs.append(np.broadcast_to(nvfp4_scale_offset(side, t, bb, D), (N, nb16)))
+        vals.append(np.asarray(fields["sb"]).astype(np.uint8))
+        return np.concatenate(offs, axis=1).astype(np.int64), np.concatenate(vals, axis=1).astype(np.uint8)
     if side == "k":
         if fmt not in ("q8_0", "fp8"):
             raise ValueError(f"K format {fmt} is not a K knob")
@@ -205,6 +257,12 @@ def read_rows(pool: np.ndarray, side: str, fmt: str, slots: np.ndarray, head: in
         hi = seg[page, o + 1].astype(np.uint16)
         return (lo | (hi << 8)).view(np.float16)
 
+    if fmt == "nvfp4":
+        off, sh = nvfp4_code_offset(side, t, j, D)
+        code = (seg[page, off].astype(np.int64) >> sh) & 0xF
+        b16 = np.arange(D // 16, dtype=np.int64).reshape(1, D // 16)
+        return {"fmt": fmt, "q": code.astype(np.uint8), "sb": seg[page, nvfp4_scale_offset(side, t, b16, D)],
+                "scale": float(np.float32(scale))}
     if side == "k":
         code = seg[page, k_code_offset(t, j, D)]
         if fmt == "q8_0":

@@ -14,6 +14,13 @@ q4_0   d = fp16_rne(max|x| / 7)            q = clamp(rne(x / d), -8, 7)
                                                                    x^ = d q
 fp8    per-tensor float32 scale s;  byte = e4m3_rne_satfinite(fp32(x) /_rn fp32(s))
                                                                    x^ = s e4m3(byte)
+nvfp4  (the card's archived "kf4" arm, an NVFP4 KV cache; reading: NVIDIA's
+       published NVFP4 block format) blocks of 16 elements, a float32
+       per-tensor scale s, an e4m3 scale byte per block and OCP FP4 E2M1 codes:
+           u   = fp32(max|x|) /_rn (6 *_rn s)            (float32 operations)
+           s_b = e4m3_rne_satfinite(u)
+           c   = e2m1_rne_satfinite(fp32(x) /_rn (e4m3(s_b) *_rn s))   (0 if s_b = 0)
+           x^  = s e4m3(s_b) e2m1(c)
 
 "rne" rounds the exact real value half-to-even.  The quotient uses the stored
 fp16 d.  With a normal fp16 d the clamps never act (|x/d| < 127.5, 7.5, 31.5);
@@ -162,6 +169,71 @@ def dequantize_fp8(b: np.ndarray, scale: float) -> np.ndarray:
     return e4m3_decode(b) * float(np.float32(scale))
 
 
+# ------------------------------------------------------- nvfp4 (e2m1) -------
+# OCP 4-bit floating point E2M1: sign bit 3, exponent bits 2..1 with bias 1,
+# mantissa bit 0; exponent 0 encodes 0 and the subnormal 0.5; no NaN or
+# infinity; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+
+NVFP4_BLOCK = 16
+E2M1_MAX = 6.0
+
+
+def e2m1_decode(code) -> np.ndarray:
+    """4-bit codes (uint8 0..15) -> float64 values."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    e = (c >> 1) & 0x3
+    mant = c & 0x1
+    val = np.where(e == 0, mant * 0.5, (1.0 + mant / 2.0) * np.exp2(e.astype(np.float64) - 1.0))
+    return sign * val
+
+
+_E2M1_CODES = np.arange(8, dtype=np.uint8)             # non-negative codes, values strictly increasing
+_E2M1_VALS = e2m1_decode(_E2M1_CODES)
+
+
+def e2m1_encode_rne_satfinite(y) -> np.ndarray:
+    """float32 values -> E2M1 codes, nearest value, ties to the even code, |y| > 6 -> 6."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    if not np.isfinite(y).all():
+        raise ValueError("non-finite input is outside the contract")
+    a = np.minimum(np.abs(y), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(_E2M1_VALS, a, side="left"), _E2M1_VALS.size - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo = a - _E2M1_VALS[lo]
+    dhi = _E2M1_VALS[hi] - a
+    pick_hi = (dhi == 0) | (dhi < dlo) | ((dhi == dlo) & (_E2M1_CODES[hi] % 2 == 0))
+    code = np.where(pick_hi, _E2M1_CODES[hi], _E2M1_CODES[lo]).astype(np.uint8)
+    return np.where(np.signbit(y), code | 0x8, code).astype(np.uint8)
+
+
+def quantize_nvfp4(x: np.ndarray, scale: float):
+    """fp16 [..., D] with float32 per-tensor scale -> (codes uint8 0..15 [..., D], scale bytes uint8 [..., D/16])."""
+    x = np.asarray(x)
+    if x.dtype != np.float16:
+        raise TypeError("quantizers take fp16 rows")
+    if x.shape[-1] % NVFP4_BLOCK:
+        raise ValueError("head_dim must be a multiple of 16")
+    xb = x.astype(np.float32).reshape(x.shape[:-1] + (x.shape[-1] // NVFP4_BLOCK, NVFP4_BLOCK))
+    if not np.isfinite(xb).all():
+        raise ValueError("non-finite input is outside the contract")
+    s = np.float32(scale)
+    amax = np.abs(xb).max(axis=-1)                                  # exact: an fp16 value
+    u = amax / (np.float32(6.0) * s)                                # float32 multiply, then float32 divide
+    sb = e4m3_encode_rne_satfinite(u.astype(np.float32))
+    eff = (e4m3_decode(sb).astype(np.float32) * s).astype(np.float32)   # float32 product
+    safe = np.where(eff > 0, eff, np.float32(1.0)).astype(np.float32)
+    y = (xb / safe[..., None]).astype(np.float32)                   # one float32 division per element
+    c = e2m1_encode_rne_satfinite(y)
+    c = np.where((sb == 0)[..., None], np.uint8(0), c).astype(np.uint8)
+    return c.reshape(x.shape), sb
+
+
+def dequantize_nvfp4(c: np.ndarray, sb: np.ndarray, scale: float) -> np.ndarray:
+    cb = e2m1_decode(c).reshape(c.shape[:-1] + (c.shape[-1] // NVFP4_BLOCK, NVFP4_BLOCK))
+    return (cb * e4m3_decode(sb)[..., None] * float(np.float32(scale))).reshape(c.shape)
+
+
 # ------------------------------------------------------ format dispatchers ---
 
 def quantize_rows(x: np.ndarray, fmt: str, scale: float = 1.0) -> dict:
@@ -177,6 +249,9 @@ def quantize_rows(x: np.ndarray, fmt: str, scale: float = 1.0) -> dict:
         return {"fmt": fmt, "q": q, "d": d}
     if fmt == "fp8":
         return {"fmt": fmt, "q": quantize_fp8(x, scale), "scale": float(np.float32(scale))}
+    if fmt == "nvfp4":
+        c, sb = quantize_nvfp4(x, scale)
+        return {"fmt": fmt, "q": c, "sb": sb, "scale": float(np.float32(scale))}
     raise ValueError(fmt)
 
 
@@ -188,6 +263,8 @@ def dequantize_rows(blk: dict) -> np.ndarray:
         return dequantize_q5_1(blk["q"], blk["d"], blk["m"])
     if fmt == "fp8":
         return dequantize_fp8(blk["q"], blk["scale"])
+    if fmt == "nvfp4":
+        return dequantize_nvfp4(blk["q"], blk["sb"], blk["scale"])
     raise ValueError(fmt)
 
 

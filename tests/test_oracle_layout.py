@@ -8,7 +8,7 @@ from oracle import layout, quant
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "layout_offsets.txt")
 
-COMBOS = [("k", "q8_0"), ("k", "fp8"), ("v", "q5_1"), ("v", "q4_0"), ("v", "fp8")]
+COMBOS = [("k", "q8_0"), ("k", "fp8"), ("k", "nvfp4"), ("v", "q5_1"), ("v", "q4_0"), ("v", "fp8"), ("v", "nvfp4")]
 
 
 def _rows(fmt, n, D, rng):
@@ -39,7 +39,7 @@ def test_pack_unpack_round_trip(side, fmt, D):
     fields = _rows(fmt, n, D, rng)
     layout.write_rows(pool, side, fields, slots, 1, D)
     back = layout.read_rows(pool, side, fmt, slots, 1, D, scale=0.0123)
-    for key in ("q", "d", "m"):
+    for key in ("q", "d", "m", "sb"):
         if key in fields:
             assert np.array_equal(back[key].view(np.uint8) if back[key].dtype == np.float16 else back[key],
                                   fields[key].view(np.uint8) if fields[key].dtype == np.float16 else fields[key])
@@ -98,5 +98,9 @@ def test_golden_offsets(row):
         assert layout.v_param_offset(t, jb, D, 8 * D) == byte
     elif what == "vfp8":
         assert layout.v_fp8_offset(t, jb, D) == byte
+    elif what in ("k4code", "v4code"):
+        assert layout.nvfp4_code_offset(what[0], t, jb, D) == (byte, int(extra))
+    elif what in ("k4scale", "v4scale"):
+        assert layout.nvfp4_scale_offset(what[0], t, jb, D) == byte
     else:
         raise AssertionError(what)

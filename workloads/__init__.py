@@ -19,7 +19,8 @@ format names).  The pages name no random generator, so the recipe is:
 * Pages are handed out sequentially unless the workload says otherwise; each
   sequence starts on a fresh page.
 * fp8 per-tensor scales are ``float32(amax / 448)`` over the whole K (resp. V)
-  tensor of the workload, passed to both sides as an input.
+  tensor of the workload, nvfp4 ones ``float32(amax / 2688)`` (6 x 448), passed
+  to both sides as an input.
 * The last ``q_len`` rows of every sequence are the rows the step appends
   (quantize-append runs inside the timed step); all other rows are written
   into the cache before timing.
@@ -37,8 +38,9 @@ import numpy as np
 PAGE_SIZE = 16
 FP8_E4M3_MAX = 448.0
 
-K_FORMATS = ("q8_0", "fp8")
-V_FORMATS = ("q5_1", "q4_0", "fp8")
+K_FORMATS = ("q8_0", "fp8", "nvfp4")
+V_FORMATS = ("q5_1", "q4_0", "fp8", "nvfp4")
+NVFP4_RANGE = 6.0 * 448.0          # largest E2M1 magnitude x largest e4m3 block scale
 
 
 @dataclass
@@ -120,14 +122,17 @@ def _amax_f16(x: np.ndarray, chunk: int = 1 << 24) -> float:
     return m
 
 
+def _tensor_scale(fmt: str, rows: np.ndarray) -> float:
+    """float32 per-tensor scale of the formats that take one (fp8, nvfp4); 1 for the others."""
+    div = {"fp8": FP8_E4M3_MAX, "nvfp4": NVFP4_RANGE}.get(fmt)
+    if div is None:
+        return 1.0
+    s = float(np.float32(_amax_f16(rows)) / np.float32(div))
+    return float(np.float32(s)) if s > 0.0 else 1.0
+
+
 def _fp8_scales(w: Workload) -> tuple[float, float]:
-    ks = float(np.float32(_amax_f16(w.k_rows)) / np.float32(FP8_E4M3_MAX)) if w.k_fmt == "fp8" else 1.0
-    vs = float(np.float32(_amax_f16(w.v_rows)) / np.float32(FP8_E4M3_MAX)) if w.v_fmt == "fp8" else 1.0
-    if w.k_fmt == "fp8" and ks == 0.0:
-        ks = 1.0
-    if w.v_fmt == "fp8" and vs == 0.0:
-        vs = 1.0
-    return float(np.float32(ks)), float(np.float32(vs))
+    return _tensor_scale(w.k_fmt, w.k_rows), _tensor_scale(w.v_fmt, w.v_rows)
 
 
 def _layout(seq_lens, shared_prefix: int, page_perm_rng=None, extra_pages: int = 0):
