@@ -32,9 +32,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-BYTES_PER_TOKEN_HEAD = {  # per token per KV head, K + V, by head_dim (quantized-KV algorithmic bytes)
-    ("q8_0", "q5_1"): 232 / 128, ("q8_0", "q4_0"): 208 / 128, ("q8_0", "fp8"): 264 / 128,
-    ("fp8", "q5_1"): 224 / 128, ("fp8", "q4_0"): 200 / 128, ("fp8", "fp8"): 256 / 128,
+# quantized-KV algorithmic bytes per element of a row: codes + block parameters
+K_BYTES_PER_ELEM = {"q8_0": 34 / 32, "fp8": 1.0, "nvfp4": 9 / 16}
+V_BYTES_PER_ELEM = {"q5_1": 24 / 32, "q4_0": 18 / 32, "fp8": 1.0, "nvfp4": 9 / 16}
+BYTES_PER_TOKEN_HEAD = {  # per token per KV head, K + V, by head_dim
+    (k, v): K_BYTES_PER_ELEM[k] + V_BYTES_PER_ELEM[v] for k in K_BYTES_PER_ELEM for v in V_BYTES_PER_ELEM
 }
 KERNEL_SOURCES = ["decode_attention_block_memra_gb300/csrc/decode_kernel.cuh",
                   "decode_attention_block_memra_gb300/csrc/memra_device.cuh",

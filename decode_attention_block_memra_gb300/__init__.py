@@ -14,7 +14,7 @@ import os
 
 from . import _build
 
-FORMATS = {"q8_0": 0, "q5_1": 1, "q4_0": 2, "fp8": 3}
+FORMATS = {"q8_0": 0, "q5_1": 1, "q4_0": 2, "fp8": 3, "nvfp4": 4}
 PAGE_SIZE = 16
 SPLIT_TOKENS = 1024
 

@@ -15,8 +15,12 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool k_format_ok(int f) { return f == MEMRA_KV_Q8_0 || f == MEMRA_KV_FP8_E4M3; }
-bool v_format_ok(int f) { return f == MEMRA_KV_Q5_1 || f == MEMRA_KV_Q4_0 || f == MEMRA_KV_FP8_E4M3; }
+bool k_format_ok(int f) { return f == MEMRA_KV_Q8_0 || f == MEMRA_KV_FP8_E4M3 || f == MEMRA_KV_NVFP4; }
+bool v_format_ok(int f) {
+  return f == MEMRA_KV_Q5_1 || f == MEMRA_KV_Q4_0 || f == MEMRA_KV_FP8_E4M3 || f == MEMRA_KV_NVFP4;
+}
+// formats with a float32 per-tensor scale
+bool scaled_format(int f) { return f == MEMRA_KV_FP8_E4M3 || f == MEMRA_KV_NVFP4; }
 
 int check_cache(const memra_kv_cache *c) {
   if (!c) return MEMRA_ERR_INVALID_ARG;
@@ -26,8 +30,8 @@ int check_cache(const memra_kv_cache *c) {
   if (c->n_kv_heads < 1 || c->num_pages < 1) return MEMRA_ERR_INVALID_ARG;
   if (!c->k_pool || !c->v_pool || !aligned16(c->k_pool) || !aligned16(c->v_pool)) return MEMRA_ERR_INVALID_ARG;
   if (c->status && (reinterpret_cast<uintptr_t>(c->status) & 3u)) return MEMRA_ERR_INVALID_ARG;
-  if (c->k_fmt == MEMRA_KV_FP8_E4M3 && !(std::isfinite(c->k_scale) && c->k_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
-  if (c->v_fmt == MEMRA_KV_FP8_E4M3 && !(std::isfinite(c->v_scale) && c->v_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
+  if (scaled_format(c->k_fmt) && !(std::isfinite(c->k_scale) && c->k_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
+  if (scaled_format(c->v_fmt) && !(std::isfinite(c->v_scale) && c->v_scale > 0.f)) return MEMRA_ERR_INVALID_ARG;
   // pools larger than 2^31 segments per head are fine (size_t offsets)
   return MEMRA_OK;
 }
@@ -189,9 +193,9 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.nsplit_max = pl.nsplit_max;
   p.num_stages = pl.num_stages;
   p.split_target = split_target(pl, c.n_kv_heads);
-  const float k_scale = c.k_fmt == MEMRA_KV_FP8_E4M3 ? c.k_scale : 1.f;
+  const float k_scale = scaled_format(c.k_fmt) ? c.k_scale : 1.f;
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
-  p.v_scale = c.v_fmt == MEMRA_KV_FP8_E4M3 ? c.v_scale : 1.f;
+  p.v_scale = scaled_format(c.v_fmt) ? c.v_scale : 1.f;
   p.k_scale = c.k_scale;
   // no position has more splits than min(ceil(L/1024), max(target, ceil(L/8192))), L its key range
   const int64_t L = longest_range(a.max_seq_len, a.window);

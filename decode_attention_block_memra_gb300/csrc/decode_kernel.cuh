@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   constexpr bool kQ4 = VF == MEMRA_KV_Q4_0;
   constexpr bool kVq = kQ5 || kQ4;
   constexpr bool kK8 = KF == MEMRA_KV_Q8_0;
+  constexpr bool kK4 = KF == MEMRA_KV_NVFP4;
+  constexpr bool kV4 = VF == MEMRA_KV_NVFP4;
   constexpr float kLazy = 2.f;
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -395,7 +397,53 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
         float sc[NT][4];
 #pragma unroll
           for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        {
+        if constexpr (kK4) {
+          // NVFP4 K: the 8 codes of each A fragment in one word; each 16-element
+          // block's e4m3 scale is folded into the fp16 codes (the product is exact)
+          uint32_t kw[2 * NB];
+#pragma unroll
+          for (int q4 = 0; q4 < NB / 2; ++q4) {
+            const uint4 x = lds128(ka + (q4 * 32 + lane) * 16);
+            kw[4 * q4] = x.x; kw[4 * q4 + 1] = x.y; kw[4 * q4 + 2] = x.z; kw[4 * q4 + 3] = x.w;
+          }
+          // block scales of tokens g and g + 8, as fp16 pairs of blocks (2 bb, 2 bb + 1)
+          uint32_t sg[NB], sg8[NB];
+          {
+            uint32_t wg[NB / 2], wg8[NB / 2];
+            if constexpr (NB == 4) {
+              const uint2 a = lds64(ka + 8 * D + g * 8), bq = lds64(ka + 8 * D + (g + 8) * 8);
+              wg[0] = a.x; wg[1] = a.y; wg8[0] = bq.x; wg8[1] = bq.y;
+            } else {
+              const uint4 a = lds128(ka + 8 * D + g * 16), bq = lds128(ka + 8 * D + (g + 8) * 16);
+              wg[0] = a.x; wg[1] = a.y; wg[2] = a.z; wg[3] = a.w;
+              wg8[0] = bq.x; wg8[1] = bq.y; wg8[2] = bq.z; wg8[3] = bq.w;
+            }
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+              sg[bb] = e4m3x2_to_half2(wg[bb / 2] >> (16 * (bb % 2)));
+              sg8[bb] = e4m3x2_to_half2(wg8[bb / 2] >> (16 * (bb % 2)));
+            }
+          }
+          const uint32_t sel = c < 2 ? 0x1010u : 0x3232u;     // the thread's 8 dims lie in block 2 bb + c / 2
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb) {
+            const uint32_t s0 = __byte_perm(sg[bb], 0u, sel), s1 = __byte_perm(sg8[bb], 0u, sel);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              const uint4 qv = lds128(qsm + ((n * NB + bb) * 32 + lane) * 16);
+#pragma unroll
+              for (int mm = 0; mm < 2; ++mm) {
+                const uint32_t w = kw[2 * bb + mm];
+                uint32_t a[4];
+                a[0] = hmul2_u32(e2m1x2_to_half2(w & 0xFFu), s0);           // token g
+                a[1] = hmul2_u32(e2m1x2_to_half2((w >> 8) & 0xFFu), s1);    // token g + 8
+                a[2] = hmul2_u32(e2m1x2_to_half2((w >> 16) & 0xFFu), s0);
+                a[3] = hmul2_u32(e2m1x2_to_half2(w >> 24), s1);
+                mma_16816(sc[n], a, mm == 0 ? qv.x : qv.z, mm == 0 ? qv.y : qv.w);
+              }
+            }
+          }
+        } else {
           uint4 kc[NB];
 #pragma unroll
             for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
@@ -624,6 +672,41 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
 #pragma unroll
               for (int n = 0; n < NT; ++n) mma_16816(mt[n], am, pb[n][0], pb[n][1]);
           }
+        } else if constexpr (kV4) {
+          // NVFP4 V: m-tile i is 16-element block i (dims 16 i + g, 16 i + g + 8).
+          // Each byte holds one token's codes of dims g and g + 8; two tokens'
+          // bytes convert to fp16 pairs and are regrouped by token pair.  The
+          // per-token block scale is folded into P (masked to 0 past the keys).
+          uint32_t sw[2 * NB];
+#pragma unroll
+          for (int q4 = 0; q4 < NB / 2; ++q4) {
+            const uint4 x = lds128(va + 8 * D + c * (2 * NB) * 4 + q4 * 16);
+            sw[4 * q4] = x.x; sw[4 * q4 + 1] = x.y; sw[4 * q4 + 2] = x.z; sw[4 * q4 + 3] = x.w;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < NB / 2; ++q4) {
+            const uint4 cw = lds128(va + (q4 * 32 + lane) * 16);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = 4 * q4 + u;
+              const uint32_t w = u == 0 ? cw.x : u == 1 ? cw.y : u == 2 ? cw.z : cw.w;
+              uint32_t s01 = e4m3x2_to_half2(sw[i] & 0xFFFFu), s89 = e4m3x2_to_half2(sw[i] >> 16);
+              if (partial) {
+                s01 &= m01;
+                s89 &= m89;
+              }
+              const uint32_t h0 = e2m1x2_to_half2(w & 0xFFu), h1 = e2m1x2_to_half2((w >> 8) & 0xFFu);
+              const uint32_t h2 = e2m1x2_to_half2((w >> 16) & 0xFFu), h3 = e2m1x2_to_half2(w >> 24);
+              uint32_t a[4];
+              a[0] = __byte_perm(h0, h1, 0x5410u);     // dim g: tokens 2c, 2c + 1
+              a[1] = __byte_perm(h0, h1, 0x7632u);     // dim g + 8
+              a[2] = __byte_perm(h2, h3, 0x5410u);     // tokens 2c + 8, 2c + 9
+              a[3] = __byte_perm(h2, h3, 0x7632u);
+#pragma unroll
+              for (int n = 0; n < NT; ++n)
+                mma_16816(o[n][i], a, hmul2_u32(pb[n][0], s01), hmul2_u32(pb[n][1], s89));
+            }
+          }
         } else {  // fp8 V
 #pragma unroll
             for (int bb = 0; bb < NB; ++bb) {
@@ -691,15 +774,14 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   for (int n = 0; n < NT; ++n) {
     const int lr0 = warp * ROWS_W + 8 * n + 2 * c;
 #pragma unroll
-    for (int bb = 0; bb < NB; ++bb) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j0 = 32 * bb + 4 * g + 2 * h;
-        mo[lr0 * D + j0] = o[n][2 * bb + h][0];
-        mo[(lr0 + 1) * D + j0] = o[n][2 * bb + h][1];
-        mo[lr0 * D + j0 + 1] = o[n][2 * bb + h][2];
-        mo[(lr0 + 1) * D + j0 + 1] = o[n][2 * bb + h][3];
-      }
+    for (int i = 0; i < 2 * NB; ++i) {
+      // dims of m-tile i's rows g and g + 8 (the V layout's dim order)
+      const int ja = kV4 ? 16 * i + g : 32 * (i / 2) + 4 * g + 2 * (i % 2);
+      const int jb = kV4 ? ja + 8 : ja + 1;
+      mo[lr0 * D + ja] = o[n][i][0];
+      mo[(lr0 + 1) * D + ja] = o[n][i][1];
+      mo[lr0 * D + jb] = o[n][i][2];
+      mo[(lr0 + 1) * D + jb] = o[n][i][3];
     }
     if (g == 0) {
       mm[lr0] = mrow[n][0];
@@ -716,7 +798,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   }
   __syncthreads();
 
-  const float vscale = VF == MEMRA_KV_FP8_E4M3 ? p.v_scale : 1.f;
+  const float vscale = p.v_scale;            // 1 unless V has a per-tensor scale
   for (int item = tid; item < nrows * (D / 4); item += kThreads) {
     const int lr = item / (D / 4);
     const int j4 = (item % (D / 4)) * 4;
@@ -773,16 +855,22 @@ cudaError_t launch_one(const DecodeParams &p, dim3 grid, size_t smem, cudaStream
 
 template <int D>
 cudaError_t dispatch_formats(int kf, int vf, const DecodeParams &p, dim3 grid, size_t smem, cudaStream_t st) {
-  if (kf == MEMRA_KV_Q8_0) {
-    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q5_1>(p, grid, smem, st);
-    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_Q4_0>(p, grid, smem, st);
-    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_Q8_0, MEMRA_KV_FP8_E4M3>(p, grid, smem, st);
-  } else if (kf == MEMRA_KV_FP8_E4M3) {
-    if (vf == MEMRA_KV_Q5_1) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q5_1>(p, grid, smem, st);
-    if (vf == MEMRA_KV_Q4_0) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_Q4_0>(p, grid, smem, st);
-    if (vf == MEMRA_KV_FP8_E4M3) return launch_one<D, MEMRA_KV_FP8_E4M3, MEMRA_KV_FP8_E4M3>(p, grid, smem, st);
+  auto by_v = [&](auto kc) -> cudaError_t {
+    constexpr int K = decltype(kc)::value;
+    switch (vf) {
+      case MEMRA_KV_Q5_1: return launch_one<D, K, MEMRA_KV_Q5_1>(p, grid, smem, st);
+      case MEMRA_KV_Q4_0: return launch_one<D, K, MEMRA_KV_Q4_0>(p, grid, smem, st);
+      case MEMRA_KV_FP8_E4M3: return launch_one<D, K, MEMRA_KV_FP8_E4M3>(p, grid, smem, st);
+      case MEMRA_KV_NVFP4: return launch_one<D, K, MEMRA_KV_NVFP4>(p, grid, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  };
+  switch (kf) {
+    case MEMRA_KV_Q8_0: return by_v(std::integral_constant<int, MEMRA_KV_Q8_0>{});
+    case MEMRA_KV_FP8_E4M3: return by_v(std::integral_constant<int, MEMRA_KV_FP8_E4M3>{});
+    case MEMRA_KV_NVFP4: return by_v(std::integral_constant<int, MEMRA_KV_NVFP4>{});
+    default: return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace memra

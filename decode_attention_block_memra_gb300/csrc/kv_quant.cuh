@@ -68,6 +68,29 @@ __device__ __forceinline__ int quant_code(float hi, float lo, float d, int lo_q,
   return min(max(static_cast<int>(q0), lo_q), hi_q);
 }
 
+// NVFP4 codes of this lane's 8 elements (one half of a 16-element block; the
+// partner half is on lane l ^ 1): e4m3 block scale of max|x| / (6 s) and E2M1
+// codes of x / (scale * s), each step one float32 operation.  Returns the
+// scale byte; codes[i] holds element i's 4-bit code.
+__device__ __forceinline__ uint32_t nvfp4_half_block(const float (&x)[8], float s, uint32_t (&codes)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float u = __fdiv_rn(amax, __fmul_rn(6.f, s));
+  const uint32_t sb = __nv_cvt_float_to_fp8(u, __NV_SATFINITE, __NV_E4M3);
+  const float eff = __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sb),
+                                                                              __NV_E4M3))), s);
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    uint32_t two = 0;
+    if (sb != 0) two = float2_to_e2m1x2(__fdiv_rn(x[i + 1], eff), __fdiv_rn(x[i], eff));
+    codes[i] = two & 0xFu;
+    codes[i + 1] = two >> 4;
+  }
+  return sb;
+}
+
 // One (token, KV head) row per group of D/8 consecutive lanes; lane l of the
 // group holds elements 8l..8l+7 of the K row (rk) and of the V row (rv).
 // Every lane of the warp must call it (it shuffles within the group); only
@@ -98,7 +121,22 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
   }
 
   // ------------------------------------------------------------------ K ---
-  {
+  if (dst.k_fmt == MEMRA_KV_NVFP4) {
+    uint8_t *seg = dst.k_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * k_seg_bytes(dst.k_fmt, D);
+    uint32_t code[8];
+    const uint32_t sb = nvfp4_half_block(xk, dst.k_scale, code);
+    // this lane holds elements 8 l .. 8 l + 7: c = l % 4 of 32-element block l / 4, in 16-block l / 2
+    const int lane_k = 4 * (t % 8) + l % 4;
+    if (act) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {       // elements e, e + 1 share a byte
+        const int w = 2 * (l / 4) + e / 4;
+        seg[((w / 4) * 32 + lane_k) * 16 + (w % 4) * 4 + t / 8 + 2 * ((e % 4) / 2)] =
+            static_cast<uint8_t>(code[e] | (code[e + 1] << 4));
+      }
+      if (l % 2 == 0) seg[8 * D + t * (D / 16) + l / 2] = static_cast<uint8_t>(sb);
+    }
+  } else {
     uint8_t *seg = dst.k_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * k_seg_bytes(dst.k_fmt, D);
     const int tg = t % 8, tp = t / 8;
     const int chunk = (tp * (kNb / 2) + b / 2) * 32 + 4 * tg + cc;
@@ -128,7 +166,27 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
   }
 
   // ------------------------------------------------------------------ V ---
-  {
+  if (dst.v_fmt == MEMRA_KV_NVFP4) {
+    uint8_t *seg = dst.v_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * v_seg_bytes(dst.v_fmt, D);
+    uint32_t code[8];
+    const uint32_t sb = nvfp4_half_block(xv, dst.v_scale, code);
+    const int b16 = l / 2, vh = l % 2;     // this lane holds elements r = 8 vh .. 8 vh + 7 of block b16
+    // elements r and r + 8 of the block share a byte: the even lane gathers its partner's codes
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mine |= code[i] << (4 * i);
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    const int c = (t % 8) / 2;
+    if (act && vh == 0) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int lane_v = 4 * r + c;
+        seg[((b16 / 4) * 32 + lane_v) * 16 + (b16 % 4) * 4 + t % 2 + 2 * (t / 8)] =
+            static_cast<uint8_t>(code[r] | (((other >> (4 * r)) & 0xFu) << 4));
+      }
+      seg[8 * D + (c * (D / 16) + b16) * 4 + t % 2 + 2 * (t / 8)] = static_cast<uint8_t>(sb);
+    }
+  } else {
     uint8_t *seg = dst.v_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * v_seg_bytes(dst.v_fmt, D);
     const int c = (t % 8) / 2, f = t % 2, pp = t / 8, k = 2 * f + pp;
     // element i of this lane: r = 8*cc + i -> vg = 2*cc + i/4, h = (i%4)/2, s = i%2

@@ -29,12 +29,13 @@ __host__ __device__ __forceinline__ int split_tokens(int T, int target) {
 
 // Segment bytes per (format, side, head_dim); see the layout in memra.h.
 __host__ __device__ constexpr int k_seg_bytes(int fmt, int D) {
-  return fmt == MEMRA_KV_Q8_0 ? 17 * D : (fmt == MEMRA_KV_FP8_E4M3 ? 16 * D : 0);
+  return fmt == MEMRA_KV_Q8_0 ? 17 * D : fmt == MEMRA_KV_FP8_E4M3 ? 16 * D : fmt == MEMRA_KV_NVFP4 ? 9 * D : 0;
 }
 __host__ __device__ constexpr int v_seg_bytes(int fmt, int D) {
   return fmt == MEMRA_KV_Q5_1 ? 12 * D
        : fmt == MEMRA_KV_Q4_0 ? 9 * D
-       : fmt == MEMRA_KV_FP8_E4M3 ? 16 * D : 0;
+       : fmt == MEMRA_KV_FP8_E4M3 ? 16 * D
+       : fmt == MEMRA_KV_NVFP4 ? 9 * D : 0;
 }
 
 // Bound on every pipeline wait: past it the kernel flags MEMRA_DEVERR_TIMEOUT
@@ -182,6 +183,22 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_bytes) {
   __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// Two OCP E2M1 codes (bits 3..0 and 7..4 of `byte`) -> fp16x2 (low code in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_half2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// E2M1 codes of two floats, round to nearest even, saturating at +-6: `hi`'s
+// code in bits 7..4, `lo`'s in bits 3..0.
+__device__ __forceinline__ uint32_t float2_to_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

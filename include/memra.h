@@ -98,7 +98,8 @@ typedef enum {
     MEMRA_KV_Q8_0 = 0,       /* K only */
     MEMRA_KV_Q5_1 = 1,       /* V only */
     MEMRA_KV_Q4_0 = 2,       /* V only */
-    MEMRA_KV_FP8_E4M3 = 3    /* K or V */
+    MEMRA_KV_FP8_E4M3 = 3,   /* K or V */
+    MEMRA_KV_NVFP4 = 4       /* K or V: the memra-bench card's archived "kf4" NVFP4 arm */
 } memra_kv_format;
 
 /* Page size (tokens) and the bounds of the split-K plan.  A sequence of T
@@ -118,16 +119,17 @@ typedef enum {
 
 /* A paged KV cache.  Plain data; the caller owns the pools and status word. */
 typedef struct {
-    int32_t k_fmt;          /* memra_kv_format: MEMRA_KV_Q8_0 or MEMRA_KV_FP8_E4M3          */
-    int32_t v_fmt;          /* memra_kv_format: MEMRA_KV_Q5_1, MEMRA_KV_Q4_0 or _FP8_E4M3   */
+    int32_t k_fmt;          /* memra_kv_format: MEMRA_KV_Q8_0, _FP8_E4M3 or _NVFP4           */
+    int32_t v_fmt;          /* memra_kv_format: MEMRA_KV_Q5_1, _Q4_0, _FP8_E4M3 or _NVFP4    */
     int32_t page_size;      /* must be MEMRA_PAGE_SIZE                                      */
     int32_t n_kv_heads;     /* >= 1                                                          */
     int32_t head_dim;       /* 128 or 256                                                    */
     int32_t num_pages;      /* pages in each pool, >= 1                                      */
     void *k_pool;           /* device, memra_kv_pool_bytes(k_fmt, 0, ...) bytes              */
     void *v_pool;           /* device, memra_kv_pool_bytes(v_fmt, 1, ...) bytes              */
-    float k_scale;          /* fp8 K: float32 per-tensor scale s (x^ = s*e4m3); else ignored */
-    float v_scale;          /* fp8 V: same for V                                             */
+    float k_scale;          /* fp8 / nvfp4 K: float32 per-tensor scale s (x^ = s*e4m3, or
+                               s*e4m3(block scale)*e2m1); else ignored                      */
+    float v_scale;          /* fp8 / nvfp4 V: same for V                                     */
     int32_t *status;        /* device int32 the kernels OR MEMRA_DEVERR_* bits into; may be NULL */
 } memra_kv_cache;
 

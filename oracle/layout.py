@@ -27,14 +27,15 @@ V side
     q4_0 d      8 D + ((c nb + b) 4 + 2 p + f) 2
     fp8 byte    (b 32 + lane) 16 + 8 h + 2 (2 p + s) + f
 
-NVFP4 (K or V; 16-element blocks, b16 = j // 16, r = j % 16; each 32-bit word
-of a lane holds the 8 codes of one m16n8k16 A fragment, 4 bits each, and every
-byte two codes of one token)
-    K codes     lane = 4 (t % 8) + (r % 8) // 2
-                byte ((b16 // 4) 32 + lane) 16 + (b16 % 4) 4 + (t // 8) + 2 (r // 8),
-                bits 4 (r % 2) ..                          (elements r, r + 1 share a byte)
+NVFP4 (K or V; scales per 16-element block b16 = j // 16; each 32-bit word of a
+lane holds the 8 codes of one m16n8k16 A fragment, 4 bits each, and every byte
+two codes of one token)
+    K codes     b = j // 32, r = j % 32, c = r // 8, e = r % 8, lane = 4 (t % 8) + c,
+                w = 2 b + e // 4
+                byte ((w // 4) 32 + lane) 16 + (w % 4) 4 + (t // 8) + 2 ((e % 4) // 2),
+                bits 4 (e % 2) ..                          (elements e, e + 1 share a byte)
     K scales    8 D + t (D/16) + b16                       (e4m3 bytes)
-    V codes     c = (t % 8) // 2, lane = 4 (r % 8) + c
+    V codes     r = j % 16, c = (t % 8) // 2, lane = 4 (r % 8) + c
                 byte ((b16 // 4) 32 + lane) 16 + (b16 % 4) 4 + (t % 2) + 2 (t // 8),
                 bits 4 (r // 8) ..                         (elements r, r + 8 share a byte)
     V scales    8 D + (c (D/16) + b16) 4 + (t % 2) + 2 (t // 8)
@@ -123,9 +124,11 @@ def nvfp4_code_offset(side: str, t, j, D):
     """(byte, shift) of the E2M1 code of element j of token t."""
     b16, r = j // 16, j % 16
     if side == "k":
-        lane = 4 * (t % 8) + (r % 8) // 2
-        byte_in_word = t // 8 + 2 * (r // 8)
-        shift = 4 * (r % 2)
+        r32 = j % 32
+        e = r32 % 8
+        lane = 4 * (t % 8) + r32 // 8
+        w = 2 * (j // 32) + e // 4
+        return ((w // 4) * 32 + lane) * 16 + (w % 4) * 4 + t // 8 + 2 * ((e % 4) // 2), 4 * (e % 2)
     else:
         lane = 4 * (r % 8) + (t % 8) // 2
         byte_in_word = t % 2 + 2 * (t // 8)

@@ -42,6 +42,8 @@ def test_segment_and_pool_sizes(memra):
     assert memra.kv_segment_bytes("q5_1", True, D) == 12 * D
     assert memra.kv_segment_bytes("q4_0", True, 256) == 9 * 256
     assert memra.kv_segment_bytes("fp8", True, 256) == 16 * 256
+    assert memra.kv_segment_bytes("nvfp4", False, D) == 9 * D
+    assert memra.kv_segment_bytes("nvfp4", True, 256) == 9 * 256
     # K knobs are q8_0 | fp8 and V knobs q5_1 | q4_0 | fp8 only
     assert memra.kv_segment_bytes("q5_1", False, D) == 0
     assert memra.kv_segment_bytes("q8_0", True, D) == 0
@@ -49,7 +51,8 @@ def test_segment_and_pool_sizes(memra):
     assert memra.kv_pool_bytes("q8_0", False, 16384, 4, 128) == 16384 * 4 * 2176
     assert memra.kv_pool_bytes("q8_0", False, 10, 4, 128, page_size=32) == 0
     from oracle import layout
-    for side, fmt in (("k", "q8_0"), ("k", "fp8"), ("v", "q5_1"), ("v", "q4_0"), ("v", "fp8")):
+    for side, fmt in (("k", "q8_0"), ("k", "fp8"), ("k", "nvfp4"), ("v", "q5_1"), ("v", "q4_0"), ("v", "fp8"),
+                      ("v", "nvfp4")):
         for D in (128, 256):
             assert memra.kv_segment_bytes(fmt, side == "v", D) == layout.segment_bytes(side, fmt, D)
 
@@ -93,6 +96,8 @@ def test_host_validation_without_gpu(memra):
     assert L.memra_kv_append(ctypes.byref(_cache(memra, head_dim=64)), 16, 16, 16, 1, None) == 2
     assert L.memra_kv_append(ctypes.byref(_cache(memra, k_pool=4100)), 16, 16, 16, 1, None) == 1  # misaligned
     assert L.memra_kv_append(ctypes.byref(_cache(memra, k_fmt=3, k_scale=0.0)), 16, 16, 16, 1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, v_fmt=4, v_scale=float("inf"))), 16, 16, 16, 1, None) == 1
+    assert L.memra_kv_append(ctypes.byref(_cache(memra, k_fmt=5)), 16, 16, 16, 1, None) == 2      # no format 5
     assert L.memra_kv_append(ctypes.byref(_cache(memra)), 16, 16, 16, -1, None) == 1
     assert L.memra_kv_append(ctypes.byref(_cache(memra)), 0, 16, 16, 1, None) == 1
     assert L.memra_kv_append(ctypes.byref(_cache(memra)), 16, 16, 16, 0, None) == 0               # no-op

@@ -48,7 +48,7 @@ def assert_rows_exact(w, res, rows, cache):
         for side, fmt, pool, scale in (("k", w.k_fmt, res.k_pool, w.k_scale), ("v", w.v_fmt, res.v_pool, w.v_scale)):
             got = layout.read_rows(pool, side, fmt, w.slots[rows], h, w.head_dim, scale)
             want = quant.select_rows(cache[side][h], rows)
-            for key in ("q", "d", "m"):
+            for key in ("q", "d", "m", "sb"):
                 if key in want:
                     a = np.asarray(got[key]).view(np.uint8)
                     b = np.asarray(want[key]).view(np.uint8)
@@ -591,3 +591,42 @@ def test_window_validation():
         memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
                           w.sm_scale, window=-3)
     assert e.value.status == 1
+
+
+# ------------------------------------------------------- NVFP4 KV (kf4 arm) --
+
+NVFP4_PAIRS = [("nvfp4", "nvfp4"), ("q8_0", "nvfp4"), ("nvfp4", "q5_1"), ("fp8", "nvfp4"), ("nvfp4", "fp8"),
+               ("nvfp4", "q4_0")]
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kf,vf", NVFP4_PAIRS)
+def test_nvfp4_formats(kf, vf, D):
+    w = W.random_case(4000 + D + 7 * NVFP4_PAIRS.index((kf, vf)), batch=3, q_len=2, n_heads=16, n_kv_heads=2,
+                      head_dim=D, k_fmt=kf, v_fmt=vf, ctx=(5, 2600))
+    res = run(w)
+    assert res.flags == 0
+    assert_pools_exact(w, res)
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_nvfp4_fused_step_and_adversarial_blocks():
+    w = W.random_case(4100, batch=4, q_len=8, n_heads=16, n_kv_heads=2, head_dim=128, k_fmt="nvfp4",
+                      v_fmt="nvfp4", ctx=(8, 700))
+    rng = np.random.default_rng(7)
+    n = w.step_rows.size * w.n_kv_heads
+    w.k_rows[w.step_rows] = _adversarial_rows(rng, n, 128).reshape(w.step_rows.size, w.n_kv_heads, 128)
+    w.v_rows[w.step_rows] = _adversarial_rows(rng, n, 128).reshape(w.step_rows.size, w.n_kv_heads, 128)
+    w.k_scale, w.v_scale = W._fp8_scales(w)
+    res = assert_fused_matches(w)
+    assert np.isfinite(res.out.astype(np.float32)).all()
+
+
+def test_nvfp4_full_size_long_context():
+    w = W.WORKLOADS["long_context"]().with_formats("nvfp4", "nvfp4")
+    cache = attention.quantize_cache(w)
+    res = run(w)
+    assert res.flags == 0
+    rows = np.union1d(np.random.default_rng(4).choice(w.slots.size, 5000, replace=False), w.step_rows)
+    assert_rows_exact(w, res, rows, cache)
+    assert_out_close(w, res, attention.reference(w, cache=cache))
