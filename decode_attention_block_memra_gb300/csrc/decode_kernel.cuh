@@ -435,10 +435,11 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
               for (int mm = 0; mm < 2; ++mm) {
                 const uint32_t w = kw[2 * bb + mm];
                 uint32_t a[4];
-                a[0] = hmul2_u32(e2m1x2_to_half2(w & 0xFFu), s0);           // token g
-                a[1] = hmul2_u32(e2m1x2_to_half2((w >> 8) & 0xFFu), s1);    // token g + 8
-                a[2] = hmul2_u32(e2m1x2_to_half2((w >> 16) & 0xFFu), s0);
-                a[3] = hmul2_u32(e2m1x2_to_half2(w >> 24), s1);
+                e2m1x8_to_half2x4(w, a);
+                a[0] = hmul2_u32(a[0], s0);           // token g
+                a[1] = hmul2_u32(a[1], s1);           // token g + 8
+                a[2] = hmul2_u32(a[2], s0);
+                a[3] = hmul2_u32(a[3], s1);
                 mma_16816(sc[n], a, mm == 0 ? qv.x : qv.z, mm == 0 ? qv.y : qv.w);
               }
             }
@@ -695,13 +696,13 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
                 s01 &= m01;
                 s89 &= m89;
               }
-              const uint32_t h0 = e2m1x2_to_half2(w & 0xFFu), h1 = e2m1x2_to_half2((w >> 8) & 0xFFu);
-              const uint32_t h2 = e2m1x2_to_half2((w >> 16) & 0xFFu), h3 = e2m1x2_to_half2(w >> 24);
+              uint32_t h[4];
+              e2m1x8_to_half2x4(w, h);
               uint32_t a[4];
-              a[0] = __byte_perm(h0, h1, 0x5410u);     // dim g: tokens 2c, 2c + 1
-              a[1] = __byte_perm(h0, h1, 0x7632u);     // dim g + 8
-              a[2] = __byte_perm(h2, h3, 0x5410u);     // tokens 2c + 8, 2c + 9
-              a[3] = __byte_perm(h2, h3, 0x7632u);
+              a[0] = __byte_perm(h[0], h[1], 0x5410u);     // dim g: tokens 2c, 2c + 1
+              a[1] = __byte_perm(h[0], h[1], 0x7632u);     // dim g + 8
+              a[2] = __byte_perm(h[2], h[3], 0x5410u);     // tokens 2c + 8, 2c + 9
+              a[3] = __byte_perm(h[2], h[3], 0x7632u);
 #pragma unroll
               for (int n = 0; n < NT; ++n)
                 mma_16816(o[n][i], a, hmul2_u32(pb[n][0], s01), hmul2_u32(pb[n][1], s89));

@@ -192,6 +192,15 @@ __device__ __forceinline__ uint32_t e2m1x2_to_half2(uint32_t byte) {
   return r;
 }
 
+// All four bytes of `w` (eight E2M1 codes) -> four fp16x2, byte k into h[k].
+// The bytes are split with one vector move, so no shift is needed per byte.
+__device__ __forceinline__ void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
 // E2M1 codes of two floats, round to nearest even, saturating at +-6: `hi`'s
 // code in bits 7..4, `lo`'s in bits 3..0.
 __device__ __forceinline__ uint32_t float2_to_e2m1x2(float hi, float lo) {
