@@ -147,8 +147,7 @@ __device__ __forceinline__ void k_pairs(uint32_t w, uint32_t &lo, uint32_t &hi) 
     lo = __byte_perm(w, 0x64646464u, 0x4140);
     hi = __byte_perm(w, 0x64646464u, 0x4342);
   } else {
-    lo = e4m3x2_to_half2(w & 0xFFFFu);
-    hi = e4m3x2_to_half2(w >> 16);
+    e4m3x4_to_half2x2(w, lo, hi);
   }
 }
 
@@ -419,9 +418,9 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
               wg8[0] = bq.x; wg8[1] = bq.y; wg8[2] = bq.z; wg8[3] = bq.w;
             }
 #pragma unroll
-            for (int bb = 0; bb < NB; ++bb) {
-              sg[bb] = e4m3x2_to_half2(wg[bb / 2] >> (16 * (bb % 2)));
-              sg8[bb] = e4m3x2_to_half2(wg8[bb / 2] >> (16 * (bb % 2)));
+            for (int q2 = 0; q2 < NB / 2; ++q2) {
+              e4m3x4_to_half2x2(wg[q2], sg[2 * q2], sg[2 * q2 + 1]);
+              e4m3x4_to_half2x2(wg8[q2], sg8[2 * q2], sg8[2 * q2 + 1]);
             }
           }
           const uint32_t sel = c < 2 ? 0x1010u : 0x3232u;     // the thread's 8 dims lie in block 2 bb + c / 2
@@ -691,7 +690,8 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
             for (int u = 0; u < 4; ++u) {
               const int i = 4 * q4 + u;
               const uint32_t w = u == 0 ? cw.x : u == 1 ? cw.y : u == 2 ? cw.z : cw.w;
-              uint32_t s01 = e4m3x2_to_half2(sw[i] & 0xFFFFu), s89 = e4m3x2_to_half2(sw[i] >> 16);
+              uint32_t s01, s89;
+              e4m3x4_to_half2x2(sw[i], s01, s89);
               if (partial) {
                 s01 &= m01;
                 s89 &= m89;
@@ -716,10 +716,8 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
               for (int h = 0; h < 2; ++h) {
               const uint32_t w0 = h == 0 ? x.x : x.z, w1 = h == 0 ? x.y : x.w;
               uint32_t a[4];
-              a[0] = e4m3x2_to_half2(w0 & 0xFFFFu);
-              a[1] = e4m3x2_to_half2(w0 >> 16);
-              a[2] = e4m3x2_to_half2(w1 & 0xFFFFu);
-              a[3] = e4m3x2_to_half2(w1 >> 16);
+              e4m3x4_to_half2x2(w0, a[0], a[1]);
+              e4m3x4_to_half2x2(w1, a[2], a[3]);
               if (partial) {
                 a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
               }

@@ -192,6 +192,14 @@ __device__ __forceinline__ uint32_t e2m1x2_to_half2(uint32_t byte) {
   return r;
 }
 
+// Both byte pairs of `w` (four e4m3 codes) -> two fp16x2: bytes 0-1 into lo,
+// bytes 2-3 into hi, split with one vector move.
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
 // All four bytes of `w` (eight E2M1 codes) -> four fp16x2, byte k into h[k].
 // The bytes are split with one vector move, so no shift is needed per byte.
 __device__ __forceinline__ void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4]) {
