@@ -630,3 +630,21 @@ def test_nvfp4_full_size_long_context():
     rows = np.union1d(np.random.default_rng(4).choice(w.slots.size, 5000, replace=False), w.step_rows)
     assert_rows_exact(w, res, rows, cache)
     assert_out_close(w, res, attention.reference(w, cache=cache))
+
+
+# -------------------------------------------- numeric class across formats --
+
+@pytest.mark.parametrize("kf,vf,D", [("fp8", "q4_0", 128), ("nvfp4", "nvfp4", 128), ("q8_0", "fp8", 256)])
+def test_verify_rows_equal_plain_decode_other_formats(kf, vf, D):
+    w = W.make_workload("verify_fmt", batch=3, q_len=4, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt=kf, v_fmt=vf,
+                        seed=77 + D, seq_lens=[2051, 1026, 300], permute_pages=True, extra_pages=1)
+    out = _verify_vs_decode(w, fused=True)
+    assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
+
+
+@pytest.mark.parametrize("kf,vf", [("nvfp4", "q5_1"), ("fp8", "fp8")])
+def test_window_fused_step_d256(kf, vf):
+    w = W.make_window_workload("win_d256", batch=3, q_len=3, n_heads=8, n_kv_heads=2, head_dim=256, k_fmt=kf,
+                               v_fmt=vf, seed=515, seq_lens=[3000, 513, 3], window=512, permute_pages=True)
+    res = assert_fused_matches(w)
+    assert_out_close(w, res, attention.reference(w))
