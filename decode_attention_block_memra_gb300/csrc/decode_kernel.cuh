@@ -95,7 +95,6 @@ cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void 
 // Warps (page lanes) per CTA: 8 at head_dim 128, 4 at 256; 2 CTAs/SM.
 template <int D>
 constexpr int kWarpsFor = D == 128 ? 8 : 4;
-constexpr int kMaxWarps = 8;
 
 template <int D>
 struct MergeLayout {
@@ -448,7 +447,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
 #pragma unroll
             for (int rr = 0; rr < NB; ++rr) kc[rr] = lds128(ka + (rr * 32 + lane) * 16);
           // q8_0 block scales of tokens g and g+8, two fp16 per word
-          uint32_t dk0[NB / 2], dk1[NB / 2];
+          [[maybe_unused]] uint32_t dk0[NB / 2], dk1[NB / 2];
           if constexpr (kK8) {
             if constexpr (NB == 4) {
               const uint2 a = lds64(ka + 16 * D + g * NB * 2), bq = lds64(ka + 16 * D + (g + 8) * NB * 2);
@@ -599,7 +598,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
               dv[bb].y &= m89;
             }
           }
-          uint32_t hw[NB / 2];
+          [[maybe_unused]] uint32_t hw[NB / 2];
           if constexpr (kQ5) {
             if constexpr (NB == 4) {
               const uint2 x = lds64(va + 8 * D + lane * (NB / 2) * 4);

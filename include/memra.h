@@ -5,7 +5,8 @@
  * What the library computes (sources are the memra project pages):
  *   - The KV-cache formats are the knobs named on the "memra-bench" card,
  *     section "drafts/kf4/ - archived experiment": K = q8_0 | fp8,
- *     V = q5_1 | q4_0 | fp8, defaults q8_0 / q5_1.
+ *     V = q5_1 | q4_0 | fp8, defaults q8_0 / q5_1; and NVFP4 for K or V, the
+ *     NVFP4 KV-cache arm that section records as archived.
  *   - Pages are the request-sized, reusable KV allocation of the memra
  *     README ("Request reuse and admission" item of the serving surface);
  *     several page tables may point at the same page (shared prefix, the
@@ -22,6 +23,11 @@
  *   q4_0  d = fp16(max|x|/7),    q = clamp(rne(x/d), -8, 7),       x^ = d*q
  *   fp8   OCP e4m3 ("fn"): byte = rne_satfinite(fp32(x) / s), x^ = s*e4m3(byte),
  *         s a float32 per-tensor scale given in memra_kv_cache.
+ *   nvfp4 blocks of 16 elements, OCP E2M1 codes, an e4m3 scale byte per block
+ *         and the float32 per-tensor scale s, each step one float32 operation:
+ *         u = max|x| / (6*s), sb = e4m3_rne_satfinite(u),
+ *         c = e2m1_rne_satfinite(x / (e4m3(sb)*s)) (c = 0 when sb = 0),
+ *         x^ = s * e4m3(sb) * e2m1(c).
  *   A stored d of 0 gives q = 0.  Inputs must be finite.
  *
  * Attention: query row i of sequence b sits at position seq_lens[b]-q_len+i
@@ -60,8 +66,15 @@
  *   V q5_1 d: 10*D + ((c*nb + b)*4 + 2*p + f)*2,  m: 11*D + same offset
  *   V q4_0 d: 8*D + ((c*nb + b)*4 + 2*p + f)*2
  *   V fp8:    byte (b*32 + lane)*16 + 8*h + 2*(2*p + s) + f
- * Segment bytes: K q8_0 17*D, K fp8 16*D, V q5_1 12*D, V q4_0 9*D,
- * V fp8 16*D.  Every byte of a segment belongs to exactly one token, so
+ *   NVFP4 (two 4-bit codes per byte, low nibble first; b16 = j/16):
+ *     K codes: c = r/8, e = r%8, lane = 4*(t%8) + c, w = 2*b + e/4,
+ *       byte ((w/4)*32 + lane)*16 + (w%4)*4 + t/8 + 2*((e%4)/2), bits 4*(e%2) ..
+ *     K scale byte: 8*D + t*(D/16) + b16
+ *     V codes: r16 = j%16, c = (t%8)/2, lane = 4*(r16%8) + c,
+ *       byte ((b16/4)*32 + lane)*16 + (b16%4)*4 + t%2 + 2*(t/8), bits 4*(r16/8) ..
+ *     V scale byte: 8*D + (c*(D/16) + b16)*4 + t%2 + 2*(t/8)
+ * Segment bytes: K q8_0 17*D, K fp8 16*D, K nvfp4 9*D, V q5_1 12*D,
+ * V q4_0 9*D, V fp8 16*D, V nvfp4 9*D.  Every byte of a segment belongs to exactly one token, so
  * appends to different slots never touch the same byte.  The order is the
  * register-fragment order of the decode kernel's tensor-core tiles, so one
  * bulk copy per segment lands the page in shared memory ready to read with
