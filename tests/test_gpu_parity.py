@@ -648,3 +648,75 @@ def test_window_fused_step_d256(kf, vf):
                                v_fmt=vf, seed=515, seq_lens=[3000, 513, 3], window=512, permute_pages=True)
     res = assert_fused_matches(w)
     assert_out_close(w, res, attention.reference(w))
+
+
+# -------------------------------------- every fp16 value through the append --
+
+def _all_fp16_finite():
+    """Every finite fp16 value, as float16 (positive and negative, both zeros)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = bits.view(np.float16)
+    return v[np.isfinite(v)]
+
+
+def _sweep_rows(fmt, rng):
+    """Rows of 128 (4 blocks of 32) in which every finite fp16 value appears inside a block whose
+    scale it does not exceed, for about 60 block scales from subnormal to 65,504."""
+    allv = _all_fp16_finite().astype(np.float64)
+    amaxes = np.unique(np.concatenate([[2.0 ** -24, 2.0 ** -20, 6.1e-5, 65504.0, 127.0, 7.0, 1.0, 0.5],
+                                       2.0 ** rng.uniform(-14, 15.9, 52)]).astype(np.float16)).astype(np.float64)
+    blocks = []
+    for a in amaxes:
+        if fmt == "q5_1":
+            lo, hi = -a, a / 3
+            vals = allv[(allv >= lo) & (allv <= hi)]
+            head = [lo, hi]
+        else:
+            vals = allv[np.abs(allv) <= a]
+            head = [a]
+        n = 32 - len(head)
+        pad = (-len(vals)) % n
+        vals = np.concatenate([vals, np.zeros(pad)]).reshape(-1, n)
+        blk = np.concatenate([np.tile(head, (vals.shape[0], 1)), vals], axis=1)
+        blocks.append(blk)
+    blocks = np.concatenate(blocks)
+    rng.shuffle(blocks)
+    blocks = np.concatenate([blocks, np.zeros(((-len(blocks)) % 4, 32))])
+    return blocks.reshape(-1, 128).astype(np.float16)
+
+
+@pytest.mark.parametrize("fmt,side", [("q8_0", "k"), ("q4_0", "v"), ("q5_1", "v"), ("fp8", "k"), ("nvfp4", "k"),
+                                      ("nvfp4", "v")])
+def test_append_every_fp16_value_bit_exact(fmt, side):
+    """Quantize-append of every finite fp16 value, against blocks of ~60 scales, matches the oracle byte for byte."""
+    import decode_attention_block_memra_gb300 as memra
+    rng = np.random.default_rng(11)
+    rows = _sweep_rows(fmt, rng)
+    n = rows.shape[0]
+    n_pages = -(-n // 16)
+    other = np.zeros_like(rows)
+    k_rows, v_rows = (rows, other) if side == "k" else (other, rows)
+    k_fmt = fmt if side == "k" else "q8_0"
+    v_fmt = fmt if side == "v" else "q5_1"
+    scale = 1.0
+    if fmt == "fp8":
+        scale = float(np.float32(np.float32(65504.0) / np.float32(448.0)))
+    elif fmt == "nvfp4":
+        scale = float(np.float32(np.float32(65504.0) / np.float32(2688.0)))
+    cache = memra.KVCache(k_fmt, v_fmt, n_pages, 1, 128, k_scale=scale, v_scale=scale, device="cuda")
+    slots = torch.arange(n, dtype=torch.int32, device="cuda")
+    memra.kv_append(cache, torch.from_numpy(k_rows).cuda().view(n, 1, 128), torch.from_numpy(v_rows).cuda().view(n, 1, 128),
+                    slots)
+    assert memra.read_status(cache) == 0
+    pool = (cache.k_pool if side == "k" else cache.v_pool).cpu().numpy().reshape(n_pages, 1, -1)
+    fields = quant.quantize_rows(rows, fmt, scale)
+    want = np.zeros_like(pool)
+    layout.write_rows(want, side, fields, np.arange(n), 0, 128)
+    seg = pool.shape[-1]
+    written = np.zeros(n_pages * seg, bool)      # bytes of the n rows (the last page may be partly empty)
+    offs, _ = layout.row_bytes(side, fields, np.arange(n) % 16, 128)
+    written.reshape(n_pages, seg)[np.broadcast_to((np.arange(n) // 16)[:, None], offs.shape), offs] = True
+    got = pool.reshape(-1)[written]
+    exp = want.reshape(-1)[written]
+    bad = np.nonzero(got != exp)[0]
+    assert bad.size == 0, f"{bad.size} bytes differ"
