@@ -259,6 +259,15 @@ def workload_config(w) -> dict:
             "l2": "flushed between steps (256 MiB write, then read back, outside the timed events)"}
 
 
+def percentile(xs, pct):
+    """Linear-interpolated percentile of a non-empty list (numpy's default rule)."""
+    ys = sorted(xs)
+    pos = (len(ys) - 1) * pct / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,7 +452,8 @@ def main():
             "kv_gbs": world * kv_bytes * args.steps / total_s / 1e9,
             "kv_hbm_frac": world * kv_bytes * args.steps / total_s / 1e9 / peak / world,
             "kv_bytes_per_step": kv_bytes, "kv_bytes_logical_per_step": logical_kv_bytes(w),
-            "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+            "step_ms": {"median": statistics.median(step_ms), "p10": percentile(step_ms, 10),
+                        "p90": percentile(step_ms, 90), "min": min(step_ms), "max": max(step_ms)},
             "roofline": {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs", "launch_ms": statistics.mean(k2_ms),
