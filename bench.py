@@ -279,6 +279,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two-call", action="store_true",
                     help="time memra_kv_append + memra_decode_attn instead of the fused memra_decode_step")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix workloads: the cascade calls (the prefix once per KV head on tcgen05)")
     ap.add_argument("--cpu-reps", type=int, default=5)
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -341,11 +343,26 @@ def main():
     B, Q = w.batch, w.q_len
     k_new = dw.step_k.view(B, Q, w.n_kv_heads, w.head_dim)
     v_new = dw.step_v.view(B, Q, w.n_kv_heads, w.head_dim)
+    if args.cascade:
+        if not w.shared_prefix:
+            raise SystemExit("--cascade needs a workload with a shared prefix")
+        cws = torch.empty(memra.decode_attn_cascade_workspace_bytes(B, Q, w.n_heads, w.head_dim, w.max_seq_len,
+                                                                    w.shared_prefix), dtype=torch.uint8,
+                          device="cuda")
 
     def hot_path():
         # store the step's rows and attend: one memra_decode_step (split-K with
         # the rows stored inside, then the combine), or the two-call form
-        if args.two_call:
+        if args.cascade:
+            if args.two_call:
+                memra.kv_append(dw.cache, dw.step_k, dw.step_v, dw.step_slots, stream=stream)
+                memra.decode_attn_cascade(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len,
+                                          w.shared_prefix, dw.out, cws, w.sm_scale, stream=stream)
+            else:
+                memra.decode_attn_cascade(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len,
+                                          w.shared_prefix, dw.out, cws, w.sm_scale, stream=stream, k_new=k_new,
+                                          v_new=v_new)
+        elif args.two_call:
             memra.kv_append(dw.cache, dw.step_k, dw.step_v, dw.step_slots, stream=stream)
             memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
                               w.sm_scale, stream=stream)
@@ -353,7 +370,7 @@ def main():
             memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out,
                               dw.workspace, w.sm_scale, stream=stream)
 
-    launches_per_step = 3 if args.two_call else 2
+    launches_per_step = (3 if args.two_call else 2) + (1 if args.cascade else 0)
 
     def step(ev0, ev1):
         # one pass of the hot path through the public entry points, events only
@@ -363,10 +380,15 @@ def main():
         ev1.record(stream)
 
     def split_pass(ev0, ev1):
-        # the split-K kernel alone (its partials pass), for its roofline
+        # the split-K kernel alone (its partials pass), for its roofline; with
+        # --cascade the whole cascade attention (prefix pass, split-K, merge)
         ev0.record(stream)
-        memra.decode_attn_partials(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace,
-                                   w.sm_scale, stream=stream)
+        if args.cascade:
+            memra.decode_attn_cascade(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, w.shared_prefix,
+                                      dw.out, cws, w.sm_scale, stream=stream)
+        else:
+            memra.decode_attn_partials(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out,
+                                       dw.workspace, w.sm_scale, stream=stream)
         ev1.record(stream)
 
     def new_events(n):
@@ -441,7 +463,7 @@ def main():
     e2e_value = job_throughput(tokens_per_step, args.steps, world, e2e_total)
 
     if rank == 0:
-        traffic = stored_traffic(w.name)
+        traffic = None if args.cascade else stored_traffic(w.name)
         line = {
             "metric": "decode-attn tokens/s (quantized-KV GB/s, % of HBM peak)",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -454,7 +476,8 @@ def main():
             "kv_bytes_per_step": kv_bytes, "kv_bytes_logical_per_step": logical_kv_bytes(w),
             "step_ms": {"median": statistics.median(step_ms), "p10": percentile(step_ms, 10),
                         "p90": percentile(step_ms, 90), "min": min(step_ms), "max": max(step_ms)},
-            "roofline": {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+            "roofline": {"kernel": "cascade attention (prefix pass + split-K + merge)" if args.cascade
+                         else "decode_split_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs", "launch_ms": statistics.mean(k2_ms),
                          "algorithmic_bytes_per_launch": kv_bytes},
@@ -463,8 +486,8 @@ def main():
                     "ms_per_step": e2e_total / args.steps * 1e3},
             # per timed step: split-K (rows stored inside) + combine, or append + split-K + combine
             "gpu_launches": launches_per_step * args.steps,
-            "step_form": "two-call (memra_kv_append + memra_decode_attn)" if args.two_call
-            else "fused (memra_decode_step)",
+            "step_form": ("cascade " if args.cascade else "") + (
+                "two-call (memra_kv_append + memra_decode_attn)" if args.two_call else "fused (memra_decode_step)"),
             "clocks": clocks,
             "device_flags": flags,
         }

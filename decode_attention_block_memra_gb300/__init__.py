@@ -22,6 +22,7 @@ DEVERR_BAD_PAGE = 1
 DEVERR_BAD_SLOT = 2
 DEVERR_BAD_SEQ_LEN = 4
 DEVERR_TIMEOUT = 8
+DEVERR_PREFIX = 16
 
 
 class MemraError(RuntimeError):
@@ -81,6 +82,15 @@ _SIGS = {
                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
                                  [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
                                                          ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "memra_decode_attn_cascade_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 6),
+    "memra_decode_attn_cascade": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 7 +
+                                  [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                   ctypes.c_void_p]),
+    "memra_decode_step_cascade": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
+                                  [ctypes.c_int32] * 7 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
+                                                          ctypes.c_void_p, ctypes.c_void_p]),
     "memra_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
                                                  ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
                                   [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
@@ -239,6 +249,30 @@ def decode_step(cache: KVCache, k_new, v_new, q, page_table, seq_lens, max_seq_l
                                               _stream(stream)), "memra_decode_step_window")
         return
     _check(lib().memra_decode_step(a[0], _ptr(k_new), _ptr(v_new), *a[1:], _stream(stream)), "memra_decode_step")
+
+
+def decode_attn_cascade_workspace_bytes(batch: int, q_len: int, n_heads: int, head_dim: int, max_seq_len: int,
+                                        prefix_len: int) -> int:
+    return int(lib().memra_decode_attn_cascade_workspace_bytes(batch, q_len, n_heads, head_dim, max_seq_len,
+                                                               prefix_len))
+
+
+def decode_attn_cascade(cache: KVCache, q, page_table, seq_lens, max_seq_len: int, prefix_len: int, out, workspace,
+                        sm_scale=None, stream=None, k_new=None, v_new=None) -> None:
+    """memra_decode_attn_cascade (or memra_decode_step_cascade when k_new / v_new are given).
+
+    Keys 0 .. prefix_len - 1 of every sequence are the pages of page_table row
+    0's first prefix_len / 16 columns, attended once per KV head for all rows
+    on the tcgen05 tensor cores; each sequence's own keys go through the split
+    kernel; the workspace is decode_attn_cascade_workspace_bytes(...).
+    """
+    a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
+    if k_new is not None or v_new is not None:
+        _check(lib().memra_decode_step_cascade(a[0], _ptr(k_new), _ptr(v_new), *a[1:6], int(prefix_len), *a[6:],
+                                               _stream(stream)), "memra_decode_step_cascade")
+        return
+    _check(lib().memra_decode_attn_cascade(*a[:6], int(prefix_len), *a[6:], _stream(stream)),
+           "memra_decode_attn_cascade")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

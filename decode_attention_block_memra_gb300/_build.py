@@ -16,8 +16,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libmemra.so")
 
-SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128.cu", "decode_d256.cu", "noalloc.cu"]
-HEADERS = ["memra_device.cuh", "decode_kernel.cuh", "kv_quant.cuh"]
+SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128.cu", "decode_d256.cu", "noalloc.cu", "cascade.cu"]
+HEADERS = ["memra_device.cuh", "decode_kernel.cuh", "kv_quant.cuh", "cascade.cuh", "tcgen05.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "cascade.cuh"
 #include "decode_kernel.cuh"
 
 using namespace memra;
@@ -122,7 +123,26 @@ struct DecodeArgs {
   size_t workspace_bytes;
   void *out;
   int32_t window;     // sliding window (tokens); > 0 also makes page_table rows rings
+  int32_t prefix = 0; // cascade: tokens shared by every sequence, attended by the prefix pass
 };
+
+// Workspace of a cascade call: the split kernel's partials over each
+// sequence's own keys (at most max_seq_len - prefix of them), then the prefix
+// pass's partials, [rows][chunks][D] floats and [rows][chunks] lse.
+size_t cascade_parts(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, int32_t max_seq_len,
+                     int32_t prefix, size_t *suf_lse, size_t *pre_o, size_t *pre_lse) {
+  size_t sl = 0;
+  size_t suf = workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len - prefix, &sl);
+  suf = (suf + 255) & ~static_cast<size_t>(255);
+  const size_t rows = static_cast<size_t>(batch) * q_len * n_heads;
+  const size_t nch = prefix > 0 ? static_cast<size_t>(ceil_div(prefix, cascade_chunk_tokens(head_dim))) : 0;
+  size_t o = rows * nch * head_dim * sizeof(float);
+  o = (o + 255) & ~static_cast<size_t>(255);
+  if (suf_lse) *suf_lse = sl;
+  if (pre_o) *pre_o = suf;
+  if (pre_lse) *pre_lse = suf + o;
+  return suf + o + rows * nch * sizeof(float);
+}
 
 // Longest key range any position of the call can have: the window (+ the part
 // of its first page before it) or the whole context.
@@ -151,7 +171,18 @@ int check_decode(const DecodeArgs &a) {
   // a ring must hold every page that the window of any query row reaches
   if (a.window > 0 && a.max_pages_per_seq < (static_cast<int64_t>(a.window) + a.q_len - 2) / kPage + 2)
     return MEMRA_ERR_INVALID_ARG;
-  const size_t need = workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, nullptr);
+  if (a.prefix < 0 || a.prefix % kPage) return MEMRA_ERR_INVALID_ARG;
+  if (a.prefix > 0) {
+    // every query row must see the whole prefix; its pages must be in the table
+    if (a.window > 0) return MEMRA_ERR_UNSUPPORTED;
+    if (a.prefix > static_cast<int64_t>(a.max_seq_len) - a.q_len || a.prefix / kPage > a.max_pages_per_seq)
+      return MEMRA_ERR_INVALID_ARG;
+    const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * (a.n_heads / a.n_kv_heads);
+    if (ceil_div(rows, 128) > 65535) return MEMRA_ERR_UNSUPPORTED;
+  }
+  const size_t need = a.prefix > 0 ? cascade_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, a.prefix,
+                                                   nullptr, nullptr, nullptr)
+                                   : workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, nullptr);
   if (a.workspace_bytes < need) return MEMRA_ERR_WORKSPACE;
   if (need > 0 && (!a.workspace || !aligned16(a.workspace))) return MEMRA_ERR_INVALID_ARG;
   return MEMRA_OK;
@@ -164,9 +195,12 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   const int group = a.n_heads / a.n_kv_heads;
   int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl);
   if (rc) return rc;
-  if (pl.nsplit_max == 0) return MEMRA_OK;    // every sequence is empty; the combine writes zeros
+  // keys this pass covers: all of them, or (cascade) those from the prefix end on
+  const int32_t range_max = a.max_seq_len - a.prefix;
+  const int nsplit_max = static_cast<int>(ceil_div(range_max, kSplitTokens));
+  if (nsplit_max == 0) return MEMRA_OK;       // every sequence is empty; the combine writes zeros
   size_t lse_off = 0;
-  workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, &lse_off);
+  workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, range_max, &lse_off);
   DecodeParams p;
   p.k_pool = static_cast<const uint8_t *>(c.k_pool);
   p.v_pool = static_cast<const uint8_t *>(c.v_pool);
@@ -187,10 +221,11 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.n_heads = a.n_heads;
   p.group = group;
   p.window = a.window;
+  p.skip = a.prefix;
   p.ring = a.window > 0 ? 1 : 0;
   p.ngh = pl.ngh;
   p.ngh_q = pl.ngh_q;
-  p.nsplit_max = pl.nsplit_max;
+  p.nsplit_max = nsplit_max;
   p.num_stages = pl.num_stages;
   p.split_target = split_target(pl, c.n_kv_heads);
   const float k_scale = scaled_format(c.k_fmt) ? c.k_scale : 1.f;
@@ -198,7 +233,7 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.v_scale = scaled_format(c.v_fmt) ? c.v_scale : 1.f;
   p.k_scale = c.k_scale;
   // no position has more splits than min(ceil(L/1024), max(target, ceil(L/8192))), L its key range
-  const int64_t L = longest_range(a.max_seq_len, a.window);
+  const int64_t L = a.prefix > 0 ? range_max : longest_range(a.max_seq_len, a.window);
   const int64_t most = std::min<int64_t>(ceil_div(L, kSplitTokens),
                                          std::max<int64_t>(p.split_target, ceil_div(L, kSplitTokensMax)));
   // x: split-major, then query position and head group (the CTAs that read
@@ -319,9 +354,106 @@ int decode_both_passes(const DecodeArgs &a, const void *k_new, const void *v_new
                      a.head_dim, a.window, a.workspace, a.out, s);
 }
 
+// Cascade: the prefix pass (tcgen05), the split kernel over each sequence's
+// own keys (with the fused append when k_new / v_new are given), the merge.
+int cascade_passes(const DecodeArgs &a, const void *k_new, const void *v_new, void *stream) {
+  if (a.prefix == 0) return decode_both_passes(a, k_new, v_new, stream);
+  int st = check_decode(a);
+  if (st || a.batch == 0) return st;
+  if (k_new || v_new) {
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return MEMRA_ERR_INVALID_ARG;
+  }
+  const memra_kv_cache &c = *a.cache;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t suf_lse = 0, pre_o = 0, pre_lse = 0;
+  cascade_parts(a.batch, a.q_len, a.n_heads, a.head_dim, a.max_seq_len, a.prefix, &suf_lse, &pre_o, &pre_lse);
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  const int group = a.n_heads / a.n_kv_heads;
+  const int n_chunks = static_cast<int>(ceil_div(a.prefix, cascade_chunk_tokens(a.head_dim)));
+
+  CascadeParams cp;
+  cp.k_pool = static_cast<const uint8_t *>(c.k_pool);
+  cp.v_pool = static_cast<const uint8_t *>(c.v_pool);
+  cp.q = static_cast<const __half *>(a.q);
+  cp.page_table = a.page_table;
+  cp.seq_lens = a.seq_lens;
+  cp.status = c.status;
+  cp.o_pre = reinterpret_cast<float *>(ws + pre_o);
+  cp.lse_pre = reinterpret_cast<float *>(ws + pre_lse);
+  cp.batch = a.batch;
+  cp.q_len = a.q_len;
+  cp.n_heads = a.n_heads;
+  cp.group = group;
+  cp.n_kv_heads = a.n_kv_heads;
+  cp.num_pages = c.num_pages;
+  cp.max_pages = a.max_pages_per_seq;
+  cp.prefix_len = a.prefix;
+  cp.n_chunks = n_chunks;
+  // staged values: q8_0 / q5_1 / q4_0 at half size, fp8 / NVFP4 without their tensor scale
+  const float k_post = c.k_fmt == MEMRA_KV_Q8_0 ? 2.f : c.k_scale;
+  cp.scale_log2 = a.sm_scale * k_post * 1.4426950408889634f;
+  cp.v_post = scaled_format(c.v_fmt) ? c.v_scale : 2.f;
+  st = cuda_status(launch_cascade_prefix(a.head_dim, c.k_fmt, c.v_fmt, cp, s));
+  if (st) return st;
+
+  st = run_partials(a, k_new, v_new, s);
+  if (st) return st;
+
+  Plan pl;
+  st = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl);
+  if (st) return st;
+  CascadeCombineParams mp;
+  mp.seq_lens = a.seq_lens;
+  mp.o_pre = cp.o_pre;
+  mp.lse_pre = cp.lse_pre;
+  mp.o_suf = reinterpret_cast<const float *>(ws);
+  mp.lse_suf = reinterpret_cast<const float *>(ws + suf_lse);
+  mp.out = static_cast<__half *>(a.out);
+  mp.status = c.status;
+  mp.rows = a.batch * a.q_len * a.n_heads;
+  mp.q_len = a.q_len;
+  mp.n_heads = a.n_heads;
+  mp.max_seq_len = a.max_seq_len;
+  mp.max_pages = a.max_pages_per_seq;
+  mp.nsplit_max = static_cast<int>(ceil_div(a.max_seq_len - a.prefix, kSplitTokens));
+  mp.split_target = split_target(pl, c.n_kv_heads);
+  mp.prefix_len = a.prefix;
+  mp.n_chunks = n_chunks;
+  return cuda_status(launch_cascade_combine(a.head_dim, mp, s));
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t memra_decode_attn_cascade_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim,
+                                                 int32_t max_seq_len, int32_t prefix_len) {
+  if (batch < 0 || q_len < 1 || n_heads < 1 || (head_dim != 128 && head_dim != 256) || max_seq_len < 0 ||
+      prefix_len < 0 || prefix_len % kPage || prefix_len > max_seq_len)
+    return 0;
+  return cascade_parts(batch, q_len, n_heads, head_dim, max_seq_len, prefix_len, nullptr, nullptr, nullptr);
+}
+
+int memra_decode_attn_cascade(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                              int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t prefix_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+                              void *stream) {
+  const DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0, prefix_len};
+  return cascade_passes(a, nullptr, nullptr, stream);
+}
+
+int memra_decode_step_cascade(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                              const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                              int32_t max_seq_len, int32_t prefix_len, int32_t batch, int32_t q_len, int32_t n_heads,
+                              int32_t n_kv_heads, int32_t head_dim, float sm_scale, void *workspace,
+                              size_t workspace_bytes, void *out, void *stream) {
+  if (!k_new || !v_new) return MEMRA_ERR_INVALID_ARG;
+  const DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+                     n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0, prefix_len};
+  return cascade_passes(a, k_new, v_new, stream);
+}
 
 int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
                       int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,

@@ -1,0 +1,696 @@
+// Cascade decode: attention over a prefix that every sequence of the call
+// shares, read and dequantized once per KV head for all of the call's query
+// rows, on the fifth-generation tensor cores.
+//
+// memra serves many requests over one shared prefix (README introduction: the
+// 4,860-token shared-prefix serving shape at concurrency 16; "Request reuse and
+// admission").  Plain decode dequantizes each shared page once per sequence.
+// Here the query rows of one KV head -- every sequence, query position and
+// query head of its group, 128 to a tile -- are the M side of tcgen05 MMAs
+// whose accumulators live in tensor memory: the one place on the decode path
+// that is a dense contraction.  The attention is exact and comes in two parts
+// merged by log-sum-exp:
+//   * the prefix pass (cascade_prefix_kernel): CTA (chunk c, KV head h, row
+//     tile) stages the chunk's 128 prefix tokens (64 at head_dim 256) with bulk
+//     copies, dequantizes K and V once into fp16 tiles in shared memory,
+//     computes S = Q K^T (M = 128 rows, N = chunk tokens, K = head_dim) into
+//     tensor memory, the softmax of each row (one thread per row and column
+//     half), P in fp16 back to shared memory, O = P V (N = head_dim, K = chunk
+//     tokens) into tensor memory, and leaves (o = O / l, lse = m + log2 l);
+//   * the split kernel over each sequence's own keys, from the prefix end on;
+//   * cascade_combine_kernel: the log-sum-exp merge of both, one CTA per row.
+//
+// Values enter the MMAs exactly: fp8 and NVFP4 codes (times their e4m3 block
+// scale) are exact in fp16, with the float32 tensor scale applied to the fp32
+// scores or output; a q8_0 / q5_1 / q4_0 value is staged at half its size as
+// an fp16 pair hi + lo (hi = fp16(x / 2), lo = fp16(x / 2 - hi), exact for
+// q8_0 and q4_0, within 2^-22 relative for q5_1's d q + m), both pairs enter
+// the same accumulator, and the factor 2 returns in fp32.  Halving keeps every
+// value of an fp16-range block finite.  A row's bytes depend on its own query
+// and the keys only (no value of one row enters another's), and on the prefix
+// length, which fixes the chunks.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "cascade.cuh"
+#include "decode_kernel.cuh"
+#include "tcgen05.cuh"
+
+namespace memra {
+namespace {
+
+constexpr int kThreads = 256;         // 8 warps: two per tensor-memory lane quarter
+constexpr int kTileRows = 128;
+constexpr uint32_t kSmemLimit = 232448;
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// fp16 of the low e4m3 byte of `byte`, broadcast to both halves.
+__device__ __forceinline__ __half2 e4m3_scale_h2(uint32_t byte) {
+  const uint32_t h = e4m3x2_to_half2(byte & 0xFFu) & 0xFFFFu;
+  return bits_h2(h | (h << 16));
+}
+
+// Raw shared-memory words of one K staging item (token t of a staged page,
+// dims 8u .. 8u + 7): the 8 code bytes (NVFP4: the 8-byte group holding the
+// item's 16 nibbles) and the block-scale bits.  Layout formulas of memra.h.
+struct KRaw {
+  uint2 w;
+  uint32_t s;
+};
+
+template <int D, int KF>
+__device__ __forceinline__ KRaw load_k8(uint32_t seg, int t, int u) {
+  constexpr int NB = D / 32;
+  const int b = u >> 2, c = u & 3;
+  const uint32_t lane = 4 * (t & 7) + c;
+  KRaw r;
+  if constexpr (KF == MEMRA_KV_NVFP4) {
+    r.w = lds64(seg + ((b >> 1) * 32 + lane) * 16 + (b & 1) * 8);
+    r.s = lds8(seg + 8 * D + t * (D / 16) + (u >> 1));
+  } else {
+    r.w = lds64(seg + (((t >> 3) * (NB / 2) + (b >> 1)) * 32 + lane) * 16 + (b & 1) * 8);
+    r.s = KF == MEMRA_KV_Q8_0 ? lds16(seg + 16 * D + (t * NB + b) * 2) : 0u;
+  }
+  return r;
+}
+
+// The item's 8 values as fp16 (hi) plus, for q8_0, the low parts (lo).
+template <int KF>
+__device__ __forceinline__ void convert_k8(const KRaw &r, int t, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+  if constexpr (KF == MEMRA_KV_Q8_0) {
+    const __half2 d2 = bits_h2(r.s | (r.s << 16));
+    const __half2 half = __float2half2_rn(0.5f), off = __float2half2_rn(-576.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // codes are stored as q + 128: splice under 1024 -> 1152 + q, then q / 2 exactly
+      const uint32_t word = k < 2 ? r.w.x : r.w.y;
+      const __half2 code = bits_h2(__byte_perm(word, 0x64646464u, k & 1 ? 0x4342 : 0x4140));
+      const __half2 qh = __hfma2(code, half, off);
+      const __half2 h = __hmul2(qh, d2);
+      hi[k] = h2_bits(h);
+      lo[k] = h2_bits(__hfma2(qh, d2, __hneg2(h)));
+    }
+  } else if constexpr (KF == MEMRA_KV_FP8_E4M3) {
+    e4m3x4_to_half2x2(r.w.x, hi[0], hi[1]);
+    e4m3x4_to_half2x2(r.w.y, hi[2], hi[3]);
+  } else {   // NVFP4: bytes t/8 and t/8 + 2 of each word hold the (2k, 2k + 1) dim pairs
+    const int sh = 8 * (t >> 3);
+    const __half2 s2 = e4m3_scale_h2(r.s);
+    hi[0] = h2_bits(__hmul2(bits_h2(e2m1x2_to_half2((r.w.x >> sh) & 0xFFu)), s2));
+    hi[1] = h2_bits(__hmul2(bits_h2(e2m1x2_to_half2((r.w.x >> (sh + 16)) & 0xFFu)), s2));
+    hi[2] = h2_bits(__hmul2(bits_h2(e2m1x2_to_half2((r.w.y >> sh) & 0xFFu)), s2));
+    hi[3] = h2_bits(__hmul2(bits_h2(e2m1x2_to_half2((r.w.y >> (sh + 16)) & 0xFFu)), s2));
+  }
+}
+
+// Raw words of one V staging task of the q5_1 / q4_0 / fp8 layouts: page half
+// ph, block b, dim group vg (dims 32 b + 4 vg .. + 3), tokens 8 ph + 2 c + f.
+struct VRaw {
+  uint2 lw[4];                 // per c: the h = 0 and h = 1 code words
+  uint32_t hw[4], dw[4], mw[4];
+};
+
+template <int D, int VF>
+__device__ __forceinline__ VRaw load_v_task(uint32_t seg, int ph, int b, int vg) {
+  constexpr int NB = D / 32;
+  VRaw r;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t lane = 4 * vg + c;
+    r.hw[c] = r.dw[c] = r.mw[c] = 0u;
+    if constexpr (VF == MEMRA_KV_FP8_E4M3) {
+      r.lw[c].x = lds32(seg + (b * 32 + lane) * 16 + 4 * ph);
+      r.lw[c].y = lds32(seg + (b * 32 + lane) * 16 + 8 + 4 * ph);
+    } else {
+      const uint32_t doff = ((c * NB + b) * 4 + 2 * ph) * 2;
+      r.lw[c] = lds64(seg + ((b >> 1) * 32 + lane) * 16 + (b & 1) * 8);
+      if constexpr (VF == MEMRA_KV_Q5_1) {
+        r.hw[c] = lds32(seg + 8 * D + (lane * (NB / 2) + (b >> 1)) * 4);
+        r.dw[c] = lds32(seg + 10 * D + doff);
+        r.mw[c] = lds32(seg + 11 * D + doff);
+      } else {
+        r.dw[c] = lds32(seg + 8 * D + doff);
+      }
+    }
+  }
+  return r;
+}
+
+// The task's values: for dim e = 2 h + s of the group, tokens 2c, 2c + 1 as one
+// fp16 pair hi[e][c] (and lo[e][c] for q5_1 / q4_0).
+template <int VF>
+__device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, uint32_t (&hi)[4][4],
+                                               uint32_t (&lo)[4][4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if constexpr (VF == MEMRA_KV_FP8_E4M3) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // bytes 2 s + f of the word: (s = 0: f = 0, 1), (s = 1: f = 0, 1)
+        e4m3x4_to_half2x2(h ? r.lw[c].y : r.lw[c].x, hi[2 * h][c], hi[2 * h + 1][c]);
+      }
+    } else {
+      float dh[2], mh[2];
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        dh[f] = 0.5f * __half2float(__ushort_as_half(static_cast<unsigned short>(r.dw[c] >> (16 * f))));
+        mh[f] = 0.5f * __half2float(__ushort_as_half(static_cast<unsigned short>(r.mw[c] >> (16 * f))));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          float x[2];
+#pragma unroll
+          for (int f = 0; f < 2; ++f) {
+            const int k = 2 * f + ph;
+            const uint32_t word = h ? r.lw[c].y : r.lw[c].x;
+            uint32_t q = (word >> (8 * k + 4 * s)) & 15u;
+            // the code as an exact float: 2^23 + q, less 2^23 (q5_1) or 2^23 + 8 (q4_0)
+            if constexpr (VF == MEMRA_KV_Q5_1) {
+              q |= ((r.hw[c] >> (8 * k + 4 * s + 2 * (b & 1) + h)) & 1u) << 4;
+              x[f] = fmaf(dh[f], __uint_as_float(0x4B000000u | q) - 8388608.f, mh[f]);
+            } else {
+              x[f] = dh[f] * (__uint_as_float(0x4B000000u | q) - 8388616.f);
+            }
+          }
+          const __half2 h2 = __floats2half2_rn(x[0], x[1]);
+          const float2 back = __half22float2(h2);
+          hi[2 * h + s][c] = h2_bits(h2);
+          lo[2 * h + s][c] = h2_bits(__floats2half2_rn(x[0] - back.x, x[1] - back.y));
+        }
+      }
+    }
+  }
+}
+
+template <int D, int KF, int VF>
+__global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const CascadeParams p) {
+  constexpr int NC = cascade_chunk_tokens(D);       // prefix tokens of this CTA
+  constexpr int NPG = NC / kPage;
+  constexpr int NB = D / 32;
+  constexpr int KSEG = k_seg_bytes(KF, D);
+  constexpr int VSEG = v_seg_bytes(VF, D);
+  constexpr bool kKLo = KF == MEMRA_KV_Q8_0;
+  constexpr bool kVLo = VF == MEMRA_KV_Q5_1 || VF == MEMRA_KV_Q4_0;
+  // shared memory (byte offsets): Q tile, K^ hi / lo (token rows), V^T hi / lo
+  // (dim rows), the raw pages, barriers.  P reuses K^ hi once S is done; the
+  // softmax exchange reuses the raw pages once V is staged; the output rows
+  // reuse Q, K^ and V^T once O is done.
+  constexpr uint32_t QB = kTileRows * D * 2, KB = NC * D * 2, VB = D * NC * 2;
+  constexpr uint32_t OFF_Q = 0, OFF_KHI = QB, OFF_KLO = OFF_KHI + KB, OFF_VHI = OFF_KLO + KB,
+                     OFF_VLO = OFF_VHI + VB, OFF_RAWK = OFF_VLO + VB, OFF_RAWV = OFF_RAWK + NPG * KSEG,
+                     OFF_BAR = OFF_RAWV + NPG * VSEG;
+  constexpr uint32_t ROWB = D * 4 + 16;             // padded output row in shared memory
+  constexpr uint32_t TCOLS = D + NC <= 256 ? 256 : 512;   // O at column 0, S at column D
+  static_assert(OFF_BAR + 64 == cascade_smem_bytes(D, KSEG, VSEG), "shared-memory plan");
+  static_assert(OFF_BAR + 64 <= kSmemLimit, "shared memory");
+  static_assert(NPG * (KSEG + VSEG) >= 2 * 2 * kTileRows * 4, "softmax exchange fits the raw pages");
+  static_assert(kTileRows * ROWB <= OFF_RAWK, "output rows fit below the raw pages");
+  static_assert(KSEG % 16 == 0 && VSEG % 16 == 0 && OFF_RAWK % 16 == 0 && OFF_BAR % 16 == 0, "alignment");
+  constexpr int QIT = kTileRows * (D / 8) / kThreads;        // Q items per thread
+  constexpr int KIT = NC * (D / 8) / kThreads;               // K items per thread
+  constexpr int VIT = VF == MEMRA_KV_NVFP4 ? NPG * 2 * (D / 16) * 8 / kThreads : NPG * 2 * NB * 8 / kThreads;
+  static_assert(QIT * kThreads == kTileRows * (D / 8) && KIT * kThreads == NC * (D / 8), "whole items");
+  static_assert((VF == MEMRA_KV_NVFP4 ? NPG * 2 * (D / 16) * 8 : NPG * 2 * NB * 8) == VIT * kThreads, "tasks");
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_addr(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar_raw = sb + OFF_BAR, bar_s = bar_raw + 8, bar_o = bar_raw + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 24);
+  int *pid_s = reinterpret_cast<int *>(smem + OFF_BAR + 32);      // NPG <= 8 page ids
+
+  const int chunk = blockIdx.x, kvh = blockIdx.y;
+  const int rows = p.batch * p.q_len * p.group;                  // query rows of one KV head
+  const int r0 = blockIdx.z * kTileRows;
+  const int tok0 = chunk * NC;
+  const int npg = min(NPG, (p.prefix_len - tok0) / kPage);       // pages of the prefix in this chunk
+  const int rows_per_seq = p.q_len * p.group;
+
+  if (warp == 0) {
+    tc::tmem_alloc(smem_addr(tmem_slot), TCOLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    mbar_init(bar_raw, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    fence_barrier_init();
+  }
+  grid_dependency_wait();          // q, the pools and the tables are written
+  allow_dependent_launch();        // the next kernel of the call may start its prologue
+
+  // This chunk's pages come from the first sequence's table.
+  int pid = -1;
+  if (tid < npg) pid = p.page_table[tok0 / kPage + tid];
+
+  // Q rows of the tile in core-matrix order: item i = (row group, 8-dim group,
+  // row in group), shared-memory byte 16 i.  All of a thread's loads are in
+  // flight together, beside the page-id load.
+  uint4 qv[QIT];
+#pragma unroll
+  for (int it = 0; it < QIT; ++it) {
+    const int i = tid + it * kThreads;
+    const int rest = i >> 3, u = rest % (D / 8);
+    const int r = r0 + (rest / (D / 8)) * 8 + (i & 7);
+    qv[it] = make_uint4(0, 0, 0, 0);
+    if (r < rows) {
+      const int b = r / rows_per_seq, rem = r % rows_per_seq;
+      const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                           rem % p.group;
+      qv[it] = *reinterpret_cast<const uint4 *>(p.q + rowid * D + 8 * u);
+    }
+  }
+  if (tid < NPG) {
+    if (tid < npg && (pid < 0 || pid >= p.num_pages)) {
+      flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+      pid = -1;
+    }
+    pid_s[tid] = pid;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0) {
+    uint32_t bytes = 0;
+    for (int i = 0; i < npg; ++i) bytes += pid_s[i] >= 0 ? KSEG + VSEG : 0;
+    if (bytes) {
+      mbar_arrive_expect_tx(bar_raw, bytes);
+      const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG, vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
+      for (int i = 0; i < npg; ++i) {
+        const int pg = pid_s[i];
+        if (pg < 0) continue;
+        bulk_copy_g2s_nohint(sb + OFF_RAWK + i * KSEG, p.k_pool + pg * kstride + static_cast<size_t>(kvh) * KSEG,
+                             KSEG, bar_raw);
+        bulk_copy_g2s_nohint(sb + OFF_RAWV + i * VSEG, p.v_pool + pg * vstride + static_cast<size_t>(kvh) * VSEG,
+                             VSEG, bar_raw);
+      }
+    } else {
+      mbar_arrive(bar_raw);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < QIT; ++it) sts128(sb + OFF_Q + 16 * (tid + it * kThreads), qv[it]);
+  // pages of this chunk that hold keys, one bit each
+  uint32_t pmask = 0;
+#pragma unroll
+  for (int i = 0; i < NPG; ++i) pmask |= (i < npg && pid_s[i] >= 0 ? 1u : 0u) << i;
+
+  bool ok = mbar_wait_bounded(bar_raw, 0, p.status);
+
+  // K^ tile (token rows, dims along K): item i = (token group, 8-dim group,
+  // token in group) at byte 16 i of each of the hi and lo tiles.  Loads first.
+  {
+    KRaw kr[KIT];
+#pragma unroll
+    for (int it = 0; it < KIT; ++it) {
+      const int i = tid + it * kThreads;
+      const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+      kr[it] = load_k8<D, KF>(sb + OFF_RAWK + (n / kPage) * KSEG, n % kPage, (i >> 3) % (D / 8));
+    }
+#pragma unroll
+    for (int it = 0; it < KIT; ++it) {
+      const int i = tid + it * kThreads;
+      const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+      uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+      if (ok && ((pmask >> (n / kPage)) & 1u)) convert_k8<KF>(kr[it], n % kPage, hi, lo);
+      sts128(sb + OFF_KHI + 16 * i, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+      if constexpr (kKLo) sts128(sb + OFF_KLO + 16 * i, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+    }
+  }
+  fence_proxy_async();             // the tiles, written by threads, are read by the tensor cores
+  tc::fence_before_sync();
+  ok = !__syncthreads_or(!ok);
+
+  constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, NC);
+  constexpr uint32_t idesc_o = tc::idesc_f16_f32(kTileRows, D);
+  if (ok && tid == 0) {
+    tc::fence_after_sync();
+    // S = Q K^T: K = head_dim in steps of 16 (256 bytes of each tile)
+#pragma unroll 1
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint64_t a = tc::smem_desc(sb + OFF_Q + 256 * ks, 128, (D / 8) * 128);
+      tc::mma_f16(tmem + D, a, tc::smem_desc(sb + OFF_KHI + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
+      if constexpr (kKLo)
+        tc::mma_f16(tmem + D, a, tc::smem_desc(sb + OFF_KLO + 256 * ks, 128, (D / 8) * 128), idesc_s, 1);
+    }
+    tc::commit(bar_s);
+  }
+
+  // V^T tiles (dim rows, tokens along K) while the score MMAs run.  A task is
+  // one staged page half (8 tokens) and a group of dims; it writes one 16-byte
+  // row of a core matrix per dim: dim dd, token group g at
+  // ((dd/8) * NC/8 + g) * 128 + (dd%8) * 16.  Loads first.
+  auto vt_store = [&](int dd, int g, uint4 h, uint4 l) {
+    const uint32_t off = ((dd >> 3) * (NC / 8) + g) * 128 + (dd & 7) * 16;
+    sts128(sb + OFF_VHI + off, h);
+    if constexpr (kVLo) sts128(sb + OFF_VLO + off, l);
+  };
+  if constexpr (VF == MEMRA_KV_NVFP4) {
+    // task (page, half, 16-dim block b16, rr): dims 16 b16 + rr and + 8
+    uint32_t cw[VIT][4], sw[VIT][4];
+#pragma unroll
+    for (int it = 0; it < VIT; ++it) {
+      const int task = tid + it * kThreads;
+      const int rr = task & 7, b16 = (task >> 3) % (D / 16), ps = task / (16 * (D / 16));
+      const uint32_t seg = sb + OFF_RAWV + ps * VSEG;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        cw[it][c] = lds32(seg + ((b16 >> 2) * 32 + 4 * rr + c) * 16 + (b16 & 3) * 4);
+        sw[it][c] = lds32(seg + 8 * D + (c * (D / 16) + b16) * 4);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < VIT; ++it) {
+      const int task = tid + it * kThreads;
+      const int rr = task & 7, b16 = (task >> 3) % (D / 16), ph = (task / (8 * (D / 16))) & 1,
+                ps = task / (16 * (D / 16));
+      uint32_t h0[4] = {0, 0, 0, 0}, h1[4] = {0, 0, 0, 0};
+      if (ok && ((pmask >> ps) & 1u)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          __half2 v[2];
+#pragma unroll
+          for (int f = 0; f < 2; ++f) {
+            const int sh = 8 * (f + 2 * ph);
+            v[f] = __hmul2(bits_h2(e2m1x2_to_half2((cw[it][c] >> sh) & 0xFFu)), e4m3_scale_h2(sw[it][c] >> sh));
+          }
+          h0[c] = h2_bits(__lows2half2(v[0], v[1]));
+          h1[c] = h2_bits(__highs2half2(v[0], v[1]));
+        }
+      }
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      vt_store(16 * b16 + rr, 2 * ps + ph, make_uint4(h0[0], h0[1], h0[2], h0[3]), z);
+      vt_store(16 * b16 + rr + 8, 2 * ps + ph, make_uint4(h1[0], h1[1], h1[2], h1[3]), z);
+    }
+  } else {
+    // task (page, half, block b, vg): dims 32 b + 4 vg + (2 h + s), tokens 8 half + 2 c + f
+    VRaw vr[VIT];
+#pragma unroll
+    for (int it = 0; it < VIT; ++it) {
+      const int task = tid + it * kThreads;
+      const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, ps = task / (16 * NB);
+      vr[it] = load_v_task<D, VF>(sb + OFF_RAWV + ps * VSEG, ph, b, vg);
+    }
+#pragma unroll
+    for (int it = 0; it < VIT; ++it) {
+      const int task = tid + it * kThreads;
+      const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, ps = task / (16 * NB);
+      uint32_t hi[4][4], lo[4][4];
+      convert_v_task<VF>(vr[it], ph, b, hi, lo);
+      const bool have = ok && ((pmask >> ps) & 1u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint4 h = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
+        const uint4 l = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
+        vt_store(32 * b + 4 * vg + e, 2 * ps + ph, h, l);
+      }
+    }
+  }
+  fence_proxy_async();
+  __syncthreads();                 // the raw pages are free: the softmax exchange goes there
+
+  // Softmax of each row: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+  // (rows), columns half (w / 4) of the chunk.
+  const int quarter = warp & 3, colh = warp >> 2;
+  const int rl = quarter * 32 + lane;
+  const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
+  float *xm = reinterpret_cast<float *>(smem + OFF_RAWK);           // [2][128] row maxima
+  float *xl = xm + 2 * kTileRows;                                     // [2][128] row sums
+  constexpr int HC = NC / 2;
+  float m_row = -INFINITY, l_row = 0.f;
+  if (ok) ok = mbar_wait_bounded(bar_s, 0, p.status);
+  ok = !__syncthreads_or(!ok);
+  if (ok) {
+    tc::fence_after_sync();
+    uint32_t sr[HC];
+#pragma unroll
+    for (int k0 = 0; k0 < HC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + D + colh * HC + k0, sr + k0);
+#pragma unroll
+    for (int k0 = 0; k0 < HC; k0 += 16) tc::wait_ld(sr + k0);
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < HC; ++k) {
+      const bool valid = (pmask >> (colh * (HC / kPage) + k / kPage)) & 1u;
+      const float v = valid ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
+      sr[k] = __float_as_uint(v);
+      mloc = fmaxf(mloc, v);
+    }
+    xm[colh * kTileRows + rl] = mloc;
+    __syncthreads();
+    m_row = fmaxf(xm[rl], xm[kTileRows + rl]);
+    // P (fp16) over K^ hi: row rl, token group g at ((rl/8) * NC/8 + g) * 128 + (rl%8) * 16
+    float lsum = 0.f;
+#pragma unroll
+    for (int g = 0; g < HC / 8; ++g) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = m_row == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[8 * g + 2 * e]) - m_row);
+        const float p1 = m_row == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[8 * g + 2 * e + 1]) - m_row);
+        const __half2 ph2 = __floats2half2_rn(p0, p1);
+        const float2 back = __half22float2(ph2);
+        lsum += back.x + back.y;
+        w4[e] = h2_bits(ph2);
+      }
+      const int gg = colh * (HC / 8) + g;
+      sts128(sb + OFF_KHI + ((rl >> 3) * (NC / 8) + gg) * 128 + (rl & 7) * 16, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+    }
+    xl[colh * kTileRows + rl] = lsum;
+    fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    l_row = xl[rl] + xl[kTileRows + rl];
+    if (tid == 0) {
+      tc::fence_after_sync();
+      // O = P V: K = chunk tokens in steps of 16
+#pragma unroll 1
+      for (int ks = 0; ks < NC / 16; ++ks) {
+        const uint64_t a = tc::smem_desc(sb + OFF_KHI + 256 * ks, 128, (NC / 8) * 128);
+        tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_VHI + 256 * ks, 128, (NC / 8) * 128), idesc_o, ks > 0);
+        if constexpr (kVLo)
+          tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_VLO + 256 * ks, 128, (NC / 8) * 128), idesc_o, 1);
+      }
+      tc::commit(bar_o);
+    }
+    ok = mbar_wait_bounded(bar_o, 0, p.status);
+  }
+  ok = !__syncthreads_or(!ok);
+
+  if (ok) {
+    tc::fence_after_sync();
+    // o = O * v_post / l into padded shared-memory rows (Q, K^, P and V^T are
+    // no longer read), then whole rows to the workspace with coalesced stores
+    const float inv = l_row > 0.f ? p.v_post / l_row : 0.f;
+#pragma unroll 1
+    for (int k0 = 0; k0 < D / 2; k0 += 32) {
+      uint32_t orr[32];
+      tc::ld_32x32b_x16(tmem + tlane + colh * (D / 2) + k0, orr);
+      tc::ld_32x32b_x16(tmem + tlane + colh * (D / 2) + k0 + 16, orr + 16);
+      tc::wait_ld(orr);
+      tc::wait_ld(orr + 16);
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        sts128(sb + OFF_Q + rl * ROWB + (colh * (D / 2) + k0 + e) * 4,
+               make_uint4(__float_as_uint(__uint_as_float(orr[e]) * inv),
+                          __float_as_uint(__uint_as_float(orr[e + 1]) * inv),
+                          __float_as_uint(__uint_as_float(orr[e + 2]) * inv),
+                          __float_as_uint(__uint_as_float(orr[e + 3]) * inv)));
+    }
+    if (colh == 0 && r0 + rl < rows) {
+      const int r = r0 + rl, b = r / rows_per_seq, rem = r % rows_per_seq;
+      const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                           rem % p.group;
+      p.lse_pre[rowid * p.n_chunks + chunk] = l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
+    }
+    __syncthreads();
+    for (int lr = warp; lr < kTileRows && r0 + lr < rows; lr += kThreads / 32) {
+      const int r = r0 + lr, b = r / rows_per_seq, rem = r % rows_per_seq;
+      const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                           rem % p.group;
+      float4 *dst = reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_chunks + chunk) * D);
+      for (int j = lane; j < D / 4; j += 32) dst[j] = *reinterpret_cast<const float4 *>(smem + OFF_Q + lr * ROWB + 16 * j);
+    }
+  }
+
+  // Every sequence of the row tile must hold the same prefix pages and see all
+  // of the prefix (flags only, off the critical path; one KV head checks).
+  if (kvh == 0) {
+    const int b_first = r0 / rows_per_seq, b_last = (min(rows, r0 + kTileRows) - 1) / rows_per_seq;
+    for (int i = tid; i < (b_last - b_first + 1) * npg; i += kThreads) {
+      const int b = b_first + i / npg, j = tok0 / kPage + i % npg;
+      if (p.page_table[static_cast<size_t>(b) * p.max_pages + j] != p.page_table[j])
+        flag_error(p.status, MEMRA_DEVERR_PREFIX);
+    }
+    if (chunk == 0)
+      for (int b = b_first + tid; b <= b_last; b += kThreads)
+        if (p.seq_lens[b] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
+}
+
+// Merge of a row's prefix-chunk partials and its own-key split partials.
+template <int D>
+__global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const CascadeCombineParams p) {
+  constexpr int PER = D / 32;
+  constexpr int W = kThreads / 32;
+  __shared__ float red[W][D];
+  __shared__ float redl[W];
+  __shared__ float mx[W];
+  grid_dependency_wait();          // both passes are complete
+  const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = row / (p.q_len * p.n_heads), qi = (row / p.n_heads) % p.q_len;
+  const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, false, p.status, false);
+  const int ns = min(key_range(Tseq, p.q_len, qi, 0, p.prefix_len, p.split_target).ns, p.nsplit_max);
+  const int parts = p.n_chunks + ns;
+  auto lse_of = [&](int k) {
+    return k < p.n_chunks ? p.lse_pre[static_cast<size_t>(row) * p.n_chunks + k]
+                          : p.lse_suf[static_cast<size_t>(row) * p.nsplit_max + (k - p.n_chunks)];
+  };
+  auto o_of = [&](int k) {
+    return k < p.n_chunks ? p.o_pre + (static_cast<size_t>(row) * p.n_chunks + k) * D
+                          : p.o_suf + (static_cast<size_t>(row) * p.nsplit_max + (k - p.n_chunks)) * D;
+  };
+  float m = -INFINITY;
+  for (int k = threadIdx.x; k < parts; k += kThreads) m = fmaxf(m, lse_of(k));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) mx[warp] = m;
+  __syncthreads();
+  float M = mx[0];
+#pragma unroll
+  for (int w = 1; w < W; ++w) M = fmaxf(M, mx[w]);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    // warp w takes parts w, w + W, ...: four of them in flight at a time
+    constexpr int BATCH = 4;
+    for (int k0 = warp; k0 < parts; k0 += BATCH * W) {
+      float ls[BATCH];
+      float4 x[BATCH][PER / 4];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int k = k0 + u * W;
+        const bool in = k < parts;
+        ls[u] = in ? lse_of(k) : -INFINITY;
+        const float4 *src = reinterpret_cast<const float4 *>(o_of(in ? k : 0) + lane * PER);
+#pragma unroll
+        for (int q4 = 0; q4 < PER / 4; ++q4) x[u][q4] = in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const float wgt = ls[u] == -INFINITY ? 0.f : fast_exp2(ls[u] - M);
+        L += wgt;
+#pragma unroll
+        for (int q4 = 0; q4 < PER / 4; ++q4) {
+          acc[4 * q4 + 0] = fmaf(wgt, x[u][q4].x, acc[4 * q4 + 0]);
+          acc[4 * q4 + 1] = fmaf(wgt, x[u][q4].y, acc[4 * q4 + 1]);
+          acc[4 * q4 + 2] = fmaf(wgt, x[u][q4].z, acc[4 * q4 + 2]);
+          acc[4 * q4 + 3] = fmaf(wgt, x[u][q4].w, acc[4 * q4 + 3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
+  if (lane == 0) redl[warp] = L;
+  __syncthreads();
+  __half *dst = p.out + static_cast<size_t>(row) * D;
+  for (int j = threadIdx.x; j < D / 2; j += kThreads) {
+    float a0 = 0.f, a1 = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      a0 += red[w][2 * j];
+      a1 += red[w][2 * j + 1];
+      l += redl[w];
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    reinterpret_cast<__half2 *>(dst)[j] = __floats2half2_rn(a0 * inv, a1 * inv);
+  }
+}
+
+template <int D, int KF, int VF>
+cudaError_t launch_prefix_one(const CascadeParams &p, cudaStream_t st) {
+  constexpr uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D));
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(cascade_prefix_kernel<D, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int rows = p.batch * p.q_len * p.group;
+  const dim3 grid(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.n_kv_heads),
+                  static_cast<unsigned>((rows + kTileRows - 1) / kTileRows));
+  return launch_pdl(cascade_prefix_kernel<D, KF, VF>, grid, dim3(kThreads), smem, st, p);
+}
+
+template <int D>
+cudaError_t prefix_formats(int kf, int vf, const CascadeParams &p, cudaStream_t st) {
+  auto by_v = [&](auto kc) -> cudaError_t {
+    constexpr int K = decltype(kc)::value;
+    switch (vf) {
+      case MEMRA_KV_Q5_1: return launch_prefix_one<D, K, MEMRA_KV_Q5_1>(p, st);
+      case MEMRA_KV_Q4_0: return launch_prefix_one<D, K, MEMRA_KV_Q4_0>(p, st);
+      case MEMRA_KV_FP8_E4M3: return launch_prefix_one<D, K, MEMRA_KV_FP8_E4M3>(p, st);
+      case MEMRA_KV_NVFP4: return launch_prefix_one<D, K, MEMRA_KV_NVFP4>(p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  };
+  switch (kf) {
+    case MEMRA_KV_Q8_0: return by_v(std::integral_constant<int, MEMRA_KV_Q8_0>{});
+    case MEMRA_KV_FP8_E4M3: return by_v(std::integral_constant<int, MEMRA_KV_FP8_E4M3>{});
+    case MEMRA_KV_NVFP4: return by_v(std::integral_constant<int, MEMRA_KV_NVFP4>{});
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cascade_prefix(int D, int kf, int vf, const CascadeParams &p, cudaStream_t st) {
+  if (p.n_chunks == 0 || p.batch == 0) return cudaSuccess;
+  return D == 128 ? prefix_formats<128>(kf, vf, p, st) : prefix_formats<256>(kf, vf, p, st);
+}
+
+cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st) {
+  if (p.rows == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(p.rows)), block(kThreads);
+  if (D == 128) return launch_pdl(cascade_combine_kernel<128>, grid, block, 0, st, p);
+  return launch_pdl(cascade_combine_kernel<256>, grid, block, 0, st, p);
+}
+
+}  // namespace memra

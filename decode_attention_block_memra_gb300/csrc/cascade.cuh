@@ -1,0 +1,52 @@
+// Cascade decode over a prefix shared by every sequence of a call: the
+// parameters of its two kernels (the prefix pass and the merge) and their
+// launchers.  The sequences' own keys go through the split kernel with
+// DecodeParams::skip = the prefix length.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "memra_device.cuh"
+
+namespace memra {
+
+// Prefix tokens one CTA of the prefix pass covers (the N of its score MMA).
+__host__ __device__ constexpr int cascade_chunk_tokens(int D) { return D == 128 ? 128 : 64; }
+
+struct CascadeParams {
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const __half *q;
+  const int32_t *page_table;
+  const int32_t *seq_lens;
+  int32_t *status;
+  float *o_pre;       // [batch * q_len * n_heads][n_chunks][D], row id (b * q_len + i) * n_heads + h
+  float *lse_pre;     // [batch * q_len * n_heads][n_chunks]
+  int batch, q_len, n_heads, group, n_kv_heads, num_pages, max_pages, prefix_len, n_chunks;
+  float scale_log2;   // sm_scale * (post-scale of the staged K values) * log2(e)
+  float v_post;       // post-scale of the staged V values
+};
+
+struct CascadeCombineParams {
+  const int32_t *seq_lens;
+  const float *o_pre;
+  const float *lse_pre;
+  const float *o_suf;     // the split kernel's partials of the keys from the prefix end on
+  const float *lse_suf;
+  __half *out;
+  int32_t *status;
+  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max, split_target, prefix_len, n_chunks;
+};
+
+// Shared memory of one prefix-pass CTA for head_dim D and the formats' segment bytes.
+__host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg) {
+  return 128u * D * 2 + 4u * cascade_chunk_tokens(D) * D * 2 +
+         static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 64u;
+}
+
+cudaError_t launch_cascade_prefix(int D, int kf, int vf, const CascadeParams &p, cudaStream_t st);
+cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st);
+
+}  // namespace memra

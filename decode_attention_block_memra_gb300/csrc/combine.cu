@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
   const int qi = (row / p.n_heads) % p.q_len;
   // keys visible to this row's position (its own split plan, as in the split kernel)
   const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.ring, p.status, false);
-  const int ns = key_range(Tseq, p.q_len, qi, p.window, p.split_target).ns;
+  const int ns = key_range(Tseq, p.q_len, qi, p.window, 0, p.split_target).ns;
   __half *dst = p.out + static_cast<size_t>(row) * D;
   if (ns == 0) {                                    // no visible key: zeros
     for (int j = threadIdx.x; j < D; j += blockDim.x) dst[j] = __float2half(0.f);

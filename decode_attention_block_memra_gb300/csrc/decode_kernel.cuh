@@ -71,6 +71,8 @@ struct DecodeParams {
   const __half *v_new;
   int n_kv_heads, num_pages, max_pages, max_seq_len, q_len, n_heads, group;
   int window;         // sliding window in tokens, 0 = none
+  int skip;           // keys below this are another pass's (a shared prefix): not read, and every
+                      // split writes its partial so that the passes can be merged
   int ring;           // 1: page_table rows are rings of max_pages columns (position p -> (p / 16) % max_pages)
   int ngh;            // groups of 8 query heads per KV head: ceil(group / 8)
   int ngh_q;          // CTAs per (split, KV head, sequence): q_len * ngh
@@ -122,20 +124,22 @@ __device__ __forceinline__ int clamp_seq_len(int T, int q_len, int max_seq_len, 
 // the combine derive it from the same numbers.
 struct KeyRange {
   int T;      // one past the last visible key (the position + 1)
-  int lo;     // first visible key (window), 0 without one
+  int lo;     // first visible key: the window's start or the skipped prefix, else 0
   int base;   // lo rounded down to its page: splits start here
   int C;      // split size
   int ns;     // splits
 };
 
-__device__ __forceinline__ KeyRange key_range(int Tseq, int q_len, int qi, int window, int split_target) {
+__device__ __forceinline__ KeyRange key_range(int Tseq, int q_len, int qi, int window, int skip,
+                                              int split_target) {
   KeyRange k;
   k.T = Tseq - q_len + qi + 1;
-  k.lo = window > 0 ? max(0, k.T - window) : 0;
+  k.lo = max(window > 0 ? k.T - window : 0, skip);
+  k.lo = max(k.lo, 0);
   k.base = k.lo & ~(kPage - 1);
   const int L = k.T - k.base;
   k.C = split_tokens(L, split_target);
-  k.ns = k.T > 0 ? (L + k.C - 1) / k.C : 0;
+  k.ns = k.T > 0 && L > 0 ? (L + k.C - 1) / k.C : 0;
   return k;
 }
 
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.ring, p.status,
                                  blockIdx.x == 0 && kvh == 0 && tid == 0);
-  const KeyRange kr = key_range(Tseq, p.q_len, qi, p.window, p.split_target);
+  const KeyRange kr = key_range(Tseq, p.q_len, qi, p.window, p.skip, p.split_target);
   const int T = kr.T, lo = kr.lo, C = kr.C;
   if (T <= 0 || split >= kr.ns) return;
   const int tok0 = kr.base + split * C;
@@ -821,7 +825,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     const int head = kvh * p.group + 8 * hg + lr;
     const size_t rowid = (static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head;
-    if (nsplit_b == 1) {
+    if (nsplit_b == 1 && p.skip == 0) {
       uint2 h;
       h.x = pack_half2(acc.x, acc.y);
       h.y = pack_half2(acc.z, acc.w);

@@ -11,7 +11,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import KVCache, decode_attn, decode_attn_workspace_bytes, decode_step, kv_append, read_status
+from . import (KVCache, decode_attn, decode_attn_cascade, decode_attn_cascade_workspace_bytes,
+               decode_attn_workspace_bytes, decode_step, kv_append, read_status)
 
 
 @dataclass
@@ -26,15 +27,35 @@ class DeviceWorkload:
     step_k: object
     step_v: object
     step_slots: object
+    cascade_workspace: object = None
 
-    def step(self, stream=None, fused: bool = False) -> None:
+    def step(self, stream=None, fused: bool = False, cascade: bool = False) -> None:
         """One pass of the hot path: append the step's rows, then attend.
 
         fused: one memra_decode_step (the split kernel stores the rows) instead
-        of memra_kv_append followed by memra_decode_attn.
+        of memra_kv_append followed by memra_decode_attn.  cascade: the
+        workload's shared prefix through the cascade calls
+        (memra_decode_step_cascade when fused, else memra_kv_append +
+        memra_decode_attn_cascade).
         """
         w = self.w
         window = getattr(w, "window", 0)
+        if cascade:
+            import torch
+            if self.cascade_workspace is None:
+                n = decode_attn_cascade_workspace_bytes(w.batch, w.q_len, w.n_heads, w.head_dim, w.max_seq_len,
+                                                        w.shared_prefix)
+                self.cascade_workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=self.q.device)
+            B, Q = w.batch, w.q_len
+            kn = vn = None
+            if fused:
+                kn = self.step_k.view(B, Q, w.n_kv_heads, w.head_dim)
+                vn = self.step_v.view(B, Q, w.n_kv_heads, w.head_dim)
+            else:
+                kv_append(self.cache, self.step_k, self.step_v, self.step_slots, stream=stream)
+            decode_attn_cascade(self.cache, self.q, self.page_table, self.seq_lens, w.max_seq_len, w.shared_prefix,
+                                self.out, self.cascade_workspace, w.sm_scale, stream=stream, k_new=kn, v_new=vn)
+            return
         if fused:
             B, Q = w.batch, w.q_len
             decode_step(self.cache, self.step_k.view(B, Q, w.n_kv_heads, w.head_dim),
@@ -91,8 +112,10 @@ class StepResult:
     initial_v_pool: np.ndarray | None = None
 
 
-def run_workload(w, fill_seed: int | None = None, want_pools: bool = False, fused: bool = False) -> StepResult:
-    """Upload, fill, run one step (fused: through memra_decode_step), copy everything back."""
+def run_workload(w, fill_seed: int | None = None, want_pools: bool = False, fused: bool = False,
+                 cascade: bool = False) -> StepResult:
+    """Upload, fill, run one step (fused: through memra_decode_step; cascade: the
+    shared-prefix cascade calls), copy everything back."""
     import torch
     init_k = init_v = None
     dw = upload(w, fill_seed=fill_seed)
@@ -101,7 +124,7 @@ def run_workload(w, fill_seed: int | None = None, want_pools: bool = False, fuse
         g = torch.Generator(device="cpu").manual_seed(fill_seed)
         init_k = torch.randint(0, 256, dw.cache.k_pool.shape, dtype=torch.uint8, generator=g).numpy()
         init_v = torch.randint(0, 256, dw.cache.v_pool.shape, dtype=torch.uint8, generator=g).numpy()
-    dw.step(fused=fused)
+    dw.step(fused=fused, cascade=cascade)
     flags = read_status(dw.cache)
     torch.cuda.synchronize()
     out = dw.out.cpu().numpy()

@@ -105,6 +105,8 @@ typedef enum {
 #define MEMRA_DEVERR_BAD_SLOT    2   /* append slot >= num_pages*16: row skipped          */
 #define MEMRA_DEVERR_BAD_SEQ_LEN 4   /* seq_len < q_len, > max_seq_len or > table: clamped */
 #define MEMRA_DEVERR_TIMEOUT     8   /* a pipeline wait gave up after ~1 s: result invalid */
+#define MEMRA_DEVERR_PREFIX     16   /* cascade: a page table differs from the first sequence's
+                                        within the shared prefix: that row used the first's pages */
 
 /* KV block formats (the memra-bench card's KV knobs). */
 typedef enum {
@@ -259,6 +261,41 @@ int memra_decode_step_window(const memra_kv_cache *cache, const void *k_new, con
                              int32_t max_seq_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
                              int32_t head_dim, float sm_scale, int32_t window, void *workspace,
                              size_t workspace_bytes, void *out, void *stream);
+
+/* Cascade decode for a prefix that every sequence of the call shares (the
+ * memra README introduction's shared-prefix serving shape: 4,860-token prompts
+ * over one shared prefix at concurrency 16).  Same arguments and result as
+ * memra_decode_attn / memra_decode_step, plus
+ *   prefix_len   a multiple of 16, <= max_seq_len - q_len: keys 0 ..
+ *                prefix_len - 1 of every sequence are the rows of the pages
+ *                page_table[0][0 .. prefix_len/16 - 1]; every row of
+ *                page_table must hold the same page ids there (a row that
+ *                does not sets MEMRA_DEVERR_PREFIX and uses the first row's
+ *                pages), and every sequence must have seq_len - q_len >=
+ *                prefix_len (else MEMRA_DEVERR_BAD_SEQ_LEN).  0 runs the plain
+ *                call.
+ * The prefix is read and dequantized once per KV head for all query rows of
+ * the call: the rows of a KV head (batch x q_len x group, 128 per tile) are
+ * the M side of tensor-core MMAs.  Each sequence's own keys go through the
+ * split kernel; a log-sum-exp merge joins both.  The result is the same
+ * attention within the output tolerance, not byte-identical to the plain
+ * call; a row's bytes depend on its own query and keys and on prefix_len
+ * only, not on the rest of the batch.  head_dim 128 or 256, no window.  The
+ * workspace is memra_decode_attn_cascade_workspace_bytes(...) (0 for invalid
+ * sizes); memra_decode_step_cascade stores the step's rows first, as
+ * memra_decode_step does. */
+size_t memra_decode_attn_cascade_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim,
+                                                 int32_t max_seq_len, int32_t prefix_len);
+int memra_decode_attn_cascade(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                              int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t prefix_len, int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+                              void *stream);
+int memra_decode_step_cascade(const memra_kv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                              const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                              int32_t max_seq_len, int32_t prefix_len, int32_t batch, int32_t q_len, int32_t n_heads,
+                              int32_t n_kv_heads, int32_t head_dim, float sm_scale, void *workspace,
+                              size_t workspace_bytes, void *out, void *stream);
 
 /* Fixed size of the device array that memra_decode_attn_noalloc uses for the
  * split-K partials (held on every device that calls it, until exit). */

@@ -117,3 +117,33 @@ def test_host_validation_without_gpu(memra):
     assert L.memra_read_status(None, None, None) == 1
     assert memra.status_string(3) == "workspace too small"
     assert memra.status_string(99) == "unknown status"
+
+
+def _cascade(memra, c, prefix, **kw):
+    a = dict(q=4096, pt=4096, maxp=4, sl=4096, maxlen=64, B=1, Q=1, Hq=8, Hkv=2, D=128, scale=0.1, ws=4096,
+             wsb=1 << 20, out=4096)
+    a.update(kw)
+    return memra.lib().memra_decode_attn_cascade(ctypes.byref(c), a["q"], a["pt"], a["maxp"], a["sl"], a["maxlen"],
+                                                 prefix, a["B"], a["Q"], a["Hq"], a["Hkv"], a["D"], a["scale"],
+                                                 a["ws"], a["wsb"], a["out"], None)
+
+
+def test_cascade_workspace_and_host_validation(memra):
+    # 16 sequences of 4,860 tokens over a 4,096-token prefix, 32 query heads
+    for D, chunk in ((128, 128), (256, 64)):
+        suf = memra.decode_attn_workspace_bytes(16, 1, 32, D, 4860 - 4096)
+        rows, chunks = 16 * 32, 4096 // chunk
+        pre_o = rows * chunks * D * 4
+        want = ((suf + 255) // 256) * 256 + ((pre_o + 255) // 256) * 256 + rows * chunks * 4
+        assert memra.decode_attn_cascade_workspace_bytes(16, 1, 32, D, 4860, 4096) == want
+    assert memra.decode_attn_cascade_workspace_bytes(16, 1, 32, 128, 4860, 4004) == 0     # not whole pages
+    assert memra.decode_attn_cascade_workspace_bytes(16, 1, 32, 128, 4860, 4880) == 0     # beyond the context
+    assert memra.decode_attn_cascade_workspace_bytes(16, 1, 32, 128, 4860, 0) >= \
+        memra.decode_attn_workspace_bytes(16, 1, 32, 128, 4860)
+    c = _cache(memra)
+    assert _cascade(memra, c, 8) == 1                       # not a multiple of 16
+    assert _cascade(memra, c, -16) == 1
+    assert _cascade(memra, c, 64) == 1                      # no key left for the new token
+    assert _cascade(memra, c, 48, wsb=10) == 3              # workspace too small
+    assert _cascade(memra, c, 80, maxlen=100) == 1          # five prefix pages, four table columns
+    assert _cascade(memra, c, 16, B=0) == 0                 # empty batch: no-op

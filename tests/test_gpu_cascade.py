@@ -1,0 +1,192 @@
+"""GPU parity of the cascade (shared-prefix) decode through the C ABI.
+
+The cascade calls compute the same attention as the plain calls: the oracle
+is the same fp64 definition over the page tables.  The prefix pass runs on
+the tcgen05 tensor cores with the rows of every sequence in one tile, so on
+top of parity the tests check that a row's bytes do not depend on the rest of
+the batch (subsets and permutations of the sequences), and that bad tables
+are flagged, not faulted.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import attention
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+ALL_PAIRS = [(k, v) for k in ("q8_0", "fp8", "nvfp4") for v in ("q5_1", "q4_0", "fp8", "nvfp4")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_attention_block_memra_gb300 import _build
+    _build.build()
+    import decode_attention_block_memra_gb300 as memra
+    memra.lib()
+
+
+def run(w, **kw):
+    from decode_attention_block_memra_gb300.runner import run_workload
+    return run_workload(w, fill_seed=1, cascade=True, **kw)
+
+
+def assert_close(w, out, ref, tol=TOL):
+    got = out.astype(np.float64)
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - ref).max()
+    assert err <= tol, f"max |gpu - oracle| = {err:.3e} > {tol}"
+    return err
+
+
+def small(kf="q8_0", vf="q5_1", D=128, q_len=1, seed=31, prefix=1024, seq_lens=(1100, 1300, 1031, 2100, 1025),
+          n_heads=16, n_kv_heads=2):
+    return W.make_workload("cascade", batch=len(seq_lens), q_len=q_len, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                           head_dim=D, k_fmt=kf, v_fmt=vf, seed=seed, seq_lens=list(seq_lens),
+                           shared_prefix=prefix)
+
+
+@pytest.mark.parametrize("kf,vf", ALL_PAIRS)
+@pytest.mark.parametrize("D", [128, 256])
+def test_cascade_formats(kf, vf, D):
+    # suffixes of 76, 276, 7, 1076 (two splits) and 1 tokens over 1,024 shared ones
+    w = small(kf, vf, D)
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_cascade_fused_step_pools_and_rows(q_len):
+    # prefix 1,040 = 8 chunks of 128 and one of 16 tokens; the step's rows are stored by the split kernel
+    w = small(q_len=q_len, prefix=1040, seq_lens=(1100, 1044, 2090, 1300), seed=32)
+    res = run(w, fused=True, want_pools=True)
+    assert res.flags == 0
+    kp, vp = attention.build_pools(w, fill=(res.initial_k_pool, res.initial_v_pool))
+    assert np.array_equal(kp, res.k_pool) and np.array_equal(vp, res.v_pool)
+    assert_close(w, res.out, attention.reference(w))
+
+
+def test_cascade_several_row_tiles():
+    # 20 sequences x q_len 2 x group 8 = 320 rows per KV head: tiles of 128, 128 and 64
+    lens = [600 + 37 * i for i in range(20)]
+    w = small(q_len=2, prefix=528, seq_lens=lens, seed=33)
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_cascade_group_and_heads(D):
+    # group 4 (2 KV heads of 4 query heads), 16 KV heads at head_dim 256
+    w = small(D=D, n_heads=8 if D == 128 else 16, n_kv_heads=2 if D == 128 else 16, q_len=3, prefix=272,
+              seq_lens=(300, 290, 1500), seed=34)
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+def test_cascade_full_size_shared_prefix():
+    w = W.shared_prefix()
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+def _device_case(w):
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w, fill_seed=1)
+    dw.step()                      # the step's rows are appended (plain path), output discarded
+    torch.cuda.synchronize()
+    return dw
+
+
+def _cascade_out(dw, idx):
+    import decode_attention_block_memra_gb300 as memra
+    w = dw.w
+    idx = torch.as_tensor(idx, dtype=torch.long, device=dw.q.device)
+    q = dw.q[idx].contiguous()
+    pt = dw.page_table[idx].contiguous()
+    sl = dw.seq_lens[idx].contiguous()
+    B = len(idx)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, memra.decode_attn_cascade_workspace_bytes(B, w.q_len, w.n_heads, w.head_dim,
+                                                                      w.max_seq_len, w.shared_prefix)),
+                     dtype=torch.uint8, device=q.device)
+    memra.decode_attn_cascade(dw.cache, q, pt, sl, w.max_seq_len, w.shared_prefix, out, ws, w.sm_scale)
+    assert memra.read_status(dw.cache) == 0
+    return out.cpu().numpy()
+
+
+def test_cascade_rows_do_not_depend_on_the_batch():
+    lens = [700 + 53 * i for i in range(18)]
+    w = small(q_len=1, prefix=640, seq_lens=lens, seed=35)        # 144 rows: two tiles
+    dw = _device_case(w)
+    full = _cascade_out(dw, list(range(18)))
+    assert_close(w, full, attention.reference(w))
+    sub = [16, 3, 9]
+    part = _cascade_out(dw, sub)
+    assert np.array_equal(part.view(np.uint16), full[sub].view(np.uint16))
+    perm = list(np.random.default_rng(0).permutation(18))
+    assert np.array_equal(_cascade_out(dw, perm).view(np.uint16), full[perm].view(np.uint16))
+    again = _cascade_out(dw, list(range(18)))
+    assert np.array_equal(again.view(np.uint16), full.view(np.uint16))
+
+
+def test_cascade_bad_tables_are_flagged_not_faulted():
+    import decode_attention_block_memra_gb300 as memra
+    w = small(prefix=512, seq_lens=(700, 800, 900), seed=36)
+    dw = _device_case(w)
+    ws = torch.empty(memra.decode_attn_cascade_workspace_bytes(w.batch, 1, w.n_heads, w.head_dim, w.max_seq_len, 512),
+                     dtype=torch.uint8, device=dw.q.device)
+    out = torch.empty_like(dw.q)
+    # a sequence whose table leaves the shared prefix
+    pt = dw.page_table.clone()
+    pt[1, 3] = pt[1, 40]
+    memra.decode_attn_cascade(dw.cache, dw.q, pt, dw.seq_lens, w.max_seq_len, 512, out, ws, w.sm_scale)
+    assert memra.read_status(dw.cache) & memra.DEVERR_PREFIX
+    # a prefix page outside the pool
+    pt = dw.page_table.clone()
+    pt[:, 5] = w.num_pages + 7
+    memra.decode_attn_cascade(dw.cache, dw.q, pt, dw.seq_lens, w.max_seq_len, 512, out, ws, w.sm_scale)
+    assert memra.read_status(dw.cache) & memra.DEVERR_BAD_PAGE
+    # a sequence shorter than the prefix plus its new token
+    sl = dw.seq_lens.clone()
+    sl[2] = 500
+    memra.decode_attn_cascade(dw.cache, dw.q, dw.page_table, sl, w.max_seq_len, 512, out, ws, w.sm_scale)
+    assert memra.read_status(dw.cache) & memra.DEVERR_BAD_SEQ_LEN
+    # the good call still matches afterwards
+    memra.decode_attn_cascade(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, 512, out, ws, w.sm_scale)
+    assert memra.read_status(dw.cache) == 0
+    assert_close(w, out.cpu().numpy(), attention.reference(w))
+
+
+def test_cascade_host_validation():
+    import decode_attention_block_memra_gb300 as memra
+    w = small(prefix=512, seq_lens=(700, 800), seed=37)
+    dw = _device_case(w)
+    L = memra.lib()
+    ws = torch.empty(memra.decode_attn_cascade_workspace_bytes(w.batch, 1, w.n_heads, w.head_dim, w.max_seq_len, 512),
+                     dtype=torch.uint8, device=dw.q.device)
+    out = torch.empty_like(dw.q)
+
+    def call(prefix, wsb=None, max_seq_len=None):
+        return L.memra_decode_attn_cascade(dw.cache.ref, dw.q.data_ptr(), dw.page_table.data_ptr(),
+                                           int(dw.page_table.shape[1]), dw.seq_lens.data_ptr(),
+                                           max_seq_len or w.max_seq_len, prefix, w.batch, 1, w.n_heads, w.n_kv_heads,
+                                           w.head_dim, ctypes.c_float(w.sm_scale), ws.data_ptr(),
+                                           ws.numel() if wsb is None else wsb, out.data_ptr(), None)
+    assert call(500) == 1                       # not a multiple of 16
+    assert call(-16) == 1
+    assert call(800) == 1                       # above max_seq_len - q_len
+    assert call(512, wsb=1000) == 3
+    assert call(512) == 0
+    assert memra.read_status(dw.cache) == 0
+    assert call(0) == 0                         # the plain call
+    assert memra.read_status(dw.cache) == 0
