@@ -41,6 +41,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MEMRA_OK : MEMRA_ERR_
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Shared memory of an SM and what the hardware reserves per resident CTA.
+constexpr size_t kSmPerSm = 228 * 1024;
+constexpr size_t kSmReservedPerCta = 1024;
+
 struct Plan {
   int ngh, ngh_q, nsplit_max, num_stages, ctas_per_sm;
   size_t smem;
@@ -76,7 +80,8 @@ size_t merge_bytes(int D) {
 // CTAs per (split, KV head, sequence) and pipeline depth.  Every query
 // position and every group of 8 query heads of a KV head gets its own CTA
 // (8 rows, one per MMA column), planned from the position's own length.
-int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan *pl) {
+// max_cta_smem caps the shared memory of one CTA (0: two CTAs per SM).
+int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan *pl, size_t max_cta_smem = 0) {
   if (q_len > MEMRA_MAX_Q_LEN || group > MEMRA_MAX_GROUP) return MEMRA_ERR_UNSUPPORTED;
   const int W = warps_for(D);
   // Pipeline depth: as many 16-token pages in flight as fit beside the other
@@ -85,7 +90,9 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
   const int ctas_per_sm = 2;
   const size_t qbytes = static_cast<size_t>(W) * (D / 32) * 512;     // warp-private Q fragments
-  const size_t budget = (226 * 1024) / ctas_per_sm - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
+  size_t cta = (226 * 1024) / ctas_per_sm;
+  if (max_cta_smem && max_cta_smem < cta) cta = max_cta_smem;
+  const size_t budget = cta - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
   int ns = static_cast<int>(budget / stage) & ~(W - 1);
   if (ns > 32) ns = 32;
   if (ns < W) ns = W;
@@ -101,10 +108,12 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   return MEMRA_OK;
 }
 
+// Partials of a split pass over ranges of at most max_seq_len keys, split no
+// finer than min_split tokens.
 size_t workspace_parts(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, int32_t max_seq_len,
-                       size_t *lse_offset) {
+                       size_t *lse_offset, int min_split = kSplitTokens) {
   const size_t rows = static_cast<size_t>(batch) * q_len * n_heads;
-  const size_t ns = static_cast<size_t>(ceil_div(max_seq_len, kSplitTokens));
+  const size_t ns = static_cast<size_t>(ceil_div(max_seq_len, min_split));
   size_t o_bytes = rows * ns * head_dim * sizeof(float);
   o_bytes = (o_bytes + 255) & ~static_cast<size_t>(255);
   if (lse_offset) *lse_offset = o_bytes;
@@ -132,7 +141,7 @@ struct DecodeArgs {
 size_t cascade_parts(int32_t batch, int32_t q_len, int32_t n_heads, int32_t head_dim, int32_t max_seq_len,
                      int32_t prefix, size_t *suf_lse, size_t *pre_o, size_t *pre_lse) {
   size_t sl = 0;
-  size_t suf = workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len - prefix, &sl);
+  size_t suf = workspace_parts(batch, q_len, n_heads, head_dim, max_seq_len - prefix, &sl, kCascadeSplitTokens);
   suf = (suf + 255) & ~static_cast<size_t>(255);
   const size_t rows = static_cast<size_t>(batch) * q_len * n_heads;
   const size_t nch = prefix > 0 ? static_cast<size_t>(ceil_div(prefix, cascade_chunk_tokens(head_dim))) : 0;
@@ -193,14 +202,22 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   const memra_kv_cache &c = *a.cache;
   Plan pl;
   const int group = a.n_heads / a.n_kv_heads;
-  int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl);
+  // a cascade call's own-key pass shares each SM with the prefix pass's CTAs
+  const int pre_per_sm = cascade_ctas_per_sm(a.head_dim);
+  const size_t cap = a.prefix > 0 ? kSmPerSm - kSmReservedPerCta * (1 + pre_per_sm) -
+                                        pre_per_sm * static_cast<size_t>(cascade_smem_bytes(
+                                                         a.head_dim, k_seg_bytes(c.k_fmt, a.head_dim),
+                                                         v_seg_bytes(c.v_fmt, a.head_dim)))
+                                  : 0;
+  int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl, cap);
   if (rc) return rc;
   // keys this pass covers: all of them, or (cascade) those from the prefix end on
   const int32_t range_max = a.max_seq_len - a.prefix;
-  const int nsplit_max = static_cast<int>(ceil_div(range_max, kSplitTokens));
+  const int min_split = a.prefix > 0 ? kCascadeSplitTokens : kSplitTokens;
+  const int nsplit_max = static_cast<int>(ceil_div(range_max, min_split));
   if (nsplit_max == 0) return MEMRA_OK;       // every sequence is empty; the combine writes zeros
   size_t lse_off = 0;
-  workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, range_max, &lse_off);
+  workspace_parts(a.batch, a.q_len, a.n_heads, a.head_dim, range_max, &lse_off, min_split);
   DecodeParams p;
   p.k_pool = static_cast<const uint8_t *>(c.k_pool);
   p.v_pool = static_cast<const uint8_t *>(c.v_pool);
@@ -232,9 +249,9 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = scaled_format(c.v_fmt) ? c.v_scale : 1.f;
   p.k_scale = c.k_scale;
-  // no position has more splits than min(ceil(L/1024), max(target, ceil(L/8192))), L its key range
+  // no position has more splits than min(ceil(L/min), max(target, ceil(L/8192))), L its key range
   const int64_t L = a.prefix > 0 ? range_max : longest_range(a.max_seq_len, a.window);
-  const int64_t most = std::min<int64_t>(ceil_div(L, kSplitTokens),
+  const int64_t most = std::min<int64_t>(ceil_div(L, min_split),
                                          std::max<int64_t>(p.split_target, ceil_div(L, kSplitTokensMax)));
   // x: split-major, then query position and head group (the CTAs that read
   // the same pages run side by side and share them through L2)
@@ -415,10 +432,10 @@ int cascade_passes(const DecodeArgs &a, const void *k_new, const void *v_new, vo
   mp.n_heads = a.n_heads;
   mp.max_seq_len = a.max_seq_len;
   mp.max_pages = a.max_pages_per_seq;
-  mp.nsplit_max = static_cast<int>(ceil_div(a.max_seq_len - a.prefix, kSplitTokens));
+  mp.nsplit_max = static_cast<int>(ceil_div(a.max_seq_len - a.prefix, kCascadeSplitTokens));
   mp.split_target = split_target(pl, c.n_kv_heads);
   mp.prefix_len = a.prefix;
-  mp.n_chunks = n_chunks;
+  mp.n_parts = cp.n_parts;
   return cuda_status(launch_cascade_combine(a.head_dim, mp, s));
 }
 

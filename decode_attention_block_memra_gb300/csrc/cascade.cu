@@ -63,6 +63,37 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr) {
   return v;
 }
 
+// Thread-block clusters: this CTA's rank, a barrier over every thread of the
+// cluster (release / acquire), and loads from a peer CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -212,34 +243,39 @@ __device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, uin
 }
 
 template <int D, int KF, int VF>
-__global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const CascadeParams p) {
+__global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_prefix_kernel(const CascadeParams p) {
   constexpr int NC = cascade_chunk_tokens(D);       // prefix tokens of this CTA
+  constexpr int H = NC / 2;                         // tokens staged at a time (one half)
   constexpr int NPG = NC / kPage;
+  constexpr int HPG = H / kPage;                    // pages of a half
   constexpr int NB = D / 32;
   constexpr int KSEG = k_seg_bytes(KF, D);
   constexpr int VSEG = v_seg_bytes(VF, D);
   constexpr bool kKLo = KF == MEMRA_KV_Q8_0;
   constexpr bool kVLo = VF == MEMRA_KV_Q5_1 || VF == MEMRA_KV_Q4_0;
-  // shared memory (byte offsets): Q tile, K^ hi / lo (token rows), V^T hi / lo
-  // (dim rows), the raw pages, barriers.  P reuses K^ hi once S is done; the
-  // softmax exchange reuses the raw pages once V is staged; the output rows
-  // reuse Q, K^ and V^T once O is done.
-  constexpr uint32_t QB = kTileRows * D * 2, KB = NC * D * 2, VB = D * NC * 2;
-  constexpr uint32_t OFF_Q = 0, OFF_KHI = QB, OFF_KLO = OFF_KHI + KB, OFF_VHI = OFF_KLO + KB,
-                     OFF_VLO = OFF_VHI + VB, OFF_RAWK = OFF_VLO + VB, OFF_RAWV = OFF_RAWK + NPG * KSEG,
-                     OFF_BAR = OFF_RAWV + NPG * VSEG;
-  constexpr uint32_t ROWB = D * 4 + 16;             // padded output row in shared memory
-  constexpr uint32_t TCOLS = D + NC <= 256 ? 256 : 512;   // O at column 0, S at column D
+  // Shared memory (byte offsets): the Q tile; one half of K^ (hi, lo; token
+  // rows) and P after the scores; one half of V^T (hi, lo; dim rows); the raw
+  // pages of the chunk (K, then V); barriers.  The softmax exchange and the
+  // row lse sit at the end of the raw K pages, which are dead once the second
+  // half of K is staged (the raw V pages are read until the end); the output
+  // rows reuse Q, K^ and V^T once O is done.
+  constexpr uint32_t QB = kTileRows * D * 2, KHB = H * D * 2, VHB = D * H * 2;
+  constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 2 * KHB, OFF_RAWK = OFF_V + 2 * VHB,
+                     OFF_RAWV = OFF_RAWK + NPG * KSEG, OFF_BAR = OFF_RAWV + NPG * VSEG;
+  constexpr uint32_t OFF_X = OFF_RAWV - 5 * kTileRows * 4;    // [2][128] max, [2][128] sum, [128] lse
+  constexpr uint32_t ROWB = D * 4 + 16;                       // padded output row in shared memory
+  constexpr uint32_t TCOLS = D + NC <= 256 ? 256 : 512;       // O at column 0, S at column D
   static_assert(OFF_BAR + 64 == cascade_smem_bytes(D, KSEG, VSEG), "shared-memory plan");
   static_assert(OFF_BAR + 64 <= kSmemLimit, "shared memory");
-  static_assert(NPG * (KSEG + VSEG) >= 2 * 2 * kTileRows * 4, "softmax exchange fits the raw pages");
-  static_assert(kTileRows * ROWB <= OFF_RAWK, "output rows fit below the raw pages");
+  static_assert(OFF_X >= OFF_RAWK && kTileRows * ROWB <= OFF_X, "output rows below the exchange");
+  static_assert(kTileRows * NC * 2 <= 2 * KHB, "P fits the K^ half");
   static_assert(KSEG % 16 == 0 && VSEG % 16 == 0 && OFF_RAWK % 16 == 0 && OFF_BAR % 16 == 0, "alignment");
   constexpr int QIT = kTileRows * (D / 8) / kThreads;        // Q items per thread
-  constexpr int KIT = NC * (D / 8) / kThreads;               // K items per thread
-  constexpr int VIT = VF == MEMRA_KV_NVFP4 ? NPG * 2 * (D / 16) * 8 / kThreads : NPG * 2 * NB * 8 / kThreads;
-  static_assert(QIT * kThreads == kTileRows * (D / 8) && KIT * kThreads == NC * (D / 8), "whole items");
-  static_assert((VF == MEMRA_KV_NVFP4 ? NPG * 2 * (D / 16) * 8 : NPG * 2 * NB * 8) == VIT * kThreads, "tasks");
+  constexpr int KIT = H * (D / 8) / kThreads;                // K items per thread and half
+  constexpr int VTASKS = VF == MEMRA_KV_NVFP4 ? HPG * 2 * (D / 16) * 8 : HPG * 2 * NB * 8;
+  constexpr int VIT = (VTASKS + kThreads - 1) / kThreads;    // V tasks per thread and half
+  static_assert(QIT * kThreads == kTileRows * (D / 8) && KIT * kThreads == H * (D / 8), "whole items");
+  static_assert(VIT * kThreads == VTASKS || (VIT == 1 && VTASKS % 32 == 0), "whole warps of tasks");
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_addr(smem);
@@ -247,6 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
   const uint32_t bar_raw = sb + OFF_BAR, bar_s = bar_raw + 8, bar_o = bar_raw + 16;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 24);
   int *pid_s = reinterpret_cast<int *>(smem + OFF_BAR + 32);      // NPG <= 8 page ids
+  float *xm = reinterpret_cast<float *>(smem + OFF_X);
+  float *xl = xm + 2 * kTileRows;
+  float *xlse = xl + 2 * kTileRows;
 
   const int chunk = blockIdx.x, kvh = blockIdx.y;
   const int rows = p.batch * p.q_len * p.group;                  // query rows of one KV head
@@ -266,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
     fence_barrier_init();
   }
   grid_dependency_wait();          // q, the pools and the tables are written
-  allow_dependent_launch();        // the next kernel of the call may start its prologue
+  allow_dependent_launch();        // the own-key split kernel may start beside this one
 
   // This chunk's pages come from the first sequence's table.
   int pid = -1;
@@ -328,128 +367,155 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
 
   bool ok = mbar_wait_bounded(bar_raw, 0, p.status);
 
-  // K^ tile (token rows, dims along K): item i = (token group, 8-dim group,
-  // token in group) at byte 16 i of each of the hi and lo tiles.  Loads first.
-  {
+  // K^ of half hf (token rows, dims along K) at the K buffer: item i =
+  // (token group, 8-dim group, token in group) at byte 16 i of hi and lo.
+  auto stage_k = [&](int hf) {
     KRaw kr[KIT];
 #pragma unroll
     for (int it = 0; it < KIT; ++it) {
       const int i = tid + it * kThreads;
-      const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+      const int n = hf * H + ((i >> 3) / (D / 8)) * 8 + (i & 7);
       kr[it] = load_k8<D, KF>(sb + OFF_RAWK + (n / kPage) * KSEG, n % kPage, (i >> 3) % (D / 8));
     }
 #pragma unroll
     for (int it = 0; it < KIT; ++it) {
       const int i = tid + it * kThreads;
-      const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+      const int n = hf * H + ((i >> 3) / (D / 8)) * 8 + (i & 7);
       uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
       if (ok && ((pmask >> (n / kPage)) & 1u)) convert_k8<KF>(kr[it], n % kPage, hi, lo);
-      sts128(sb + OFF_KHI + 16 * i, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-      if constexpr (kKLo) sts128(sb + OFF_KLO + 16 * i, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+      sts128(sb + OFF_K + 16 * i, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+      if constexpr (kKLo) sts128(sb + OFF_K + KHB + 16 * i, make_uint4(lo[0], lo[1], lo[2], lo[3]));
     }
-  }
-  fence_proxy_async();             // the tiles, written by threads, are read by the tensor cores
-  tc::fence_before_sync();
-  ok = !__syncthreads_or(!ok);
-
-  constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, NC);
+  };
+  // V^T of half hf (dim rows, tokens along K) at the V buffer: a task is one
+  // staged page half (8 tokens) and a group of dims; it writes one 16-byte row
+  // of a core matrix per dim: dim dd, token group g at ((dd/8) * H/8 + g) * 128 + (dd%8) * 16.
+  auto vt_store = [&](int dd, int g, uint4 h, uint4 l) {
+    const uint32_t off = ((dd >> 3) * (H / 8) + g) * 128 + (dd & 7) * 16;
+    sts128(sb + OFF_V + off, h);
+    if constexpr (kVLo) sts128(sb + OFF_V + VHB + off, l);
+  };
+  auto stage_v = [&](int hf) {
+    if constexpr (VF == MEMRA_KV_NVFP4) {
+      // task (page, half page, 16-dim block b16, rr): dims 16 b16 + rr and + 8
+      uint32_t cw[VIT][4], sw[VIT][4];
+#pragma unroll
+      for (int it = 0; it < VIT; ++it) {
+        const int task = tid + it * kThreads;
+        if (task >= VTASKS) break;
+        const int rr = task & 7, b16 = (task >> 3) % (D / 16), ps = hf * HPG + task / (16 * (D / 16));
+        const uint32_t seg = sb + OFF_RAWV + ps * VSEG;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          cw[it][c] = lds32(seg + ((b16 >> 2) * 32 + 4 * rr + c) * 16 + (b16 & 3) * 4);
+          sw[it][c] = lds32(seg + 8 * D + (c * (D / 16) + b16) * 4);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < VIT; ++it) {
+        const int task = tid + it * kThreads;
+        if (task >= VTASKS) break;
+        const int rr = task & 7, b16 = (task >> 3) % (D / 16), ph = (task / (8 * (D / 16))) & 1,
+                  psl = task / (16 * (D / 16));
+        uint32_t h0[4] = {0, 0, 0, 0}, h1[4] = {0, 0, 0, 0};
+        if (ok && ((pmask >> (hf * HPG + psl)) & 1u)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            __half2 v[2];
+#pragma unroll
+            for (int f = 0; f < 2; ++f) {
+              const int sh = 8 * (f + 2 * ph);
+              v[f] = __hmul2(bits_h2(e2m1x2_to_half2((cw[it][c] >> sh) & 0xFFu)), e4m3_scale_h2(sw[it][c] >> sh));
+            }
+            h0[c] = h2_bits(__lows2half2(v[0], v[1]));
+            h1[c] = h2_bits(__highs2half2(v[0], v[1]));
+          }
+        }
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        vt_store(16 * b16 + rr, 2 * psl + ph, make_uint4(h0[0], h0[1], h0[2], h0[3]), z);
+        vt_store(16 * b16 + rr + 8, 2 * psl + ph, make_uint4(h1[0], h1[1], h1[2], h1[3]), z);
+      }
+    } else {
+      // task (page, half page, block b, vg): dims 32 b + 4 vg + (2 h + s), tokens 8 half + 2 c + f
+      VRaw vr[VIT];
+#pragma unroll
+      for (int it = 0; it < VIT; ++it) {
+        const int task = tid + it * kThreads;
+        if (task >= VTASKS) break;
+        const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1,
+                  ps = hf * HPG + task / (16 * NB);
+        vr[it] = load_v_task<D, VF>(sb + OFF_RAWV + ps * VSEG, ph, b, vg);
+      }
+#pragma unroll
+      for (int it = 0; it < VIT; ++it) {
+        const int task = tid + it * kThreads;
+        if (task >= VTASKS) break;
+        const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, psl = task / (16 * NB);
+        uint32_t hi[4][4], lo[4][4];
+        convert_v_task<VF>(vr[it], ph, b, hi, lo);
+        const bool have = ok && ((pmask >> (hf * HPG + psl)) & 1u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint4 h = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
+          const uint4 l = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
+          vt_store(32 * b + 4 * vg + e, 2 * psl + ph, h, l);
+        }
+      }
+    }
+  };
+  // S[:, half hf] = Q K^T (N = H tokens, K = head_dim in steps of 16), into
+  // tensor-memory columns D + hf * H ..
+  constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, H);
   constexpr uint32_t idesc_o = tc::idesc_f16_f32(kTileRows, D);
-  if (ok && tid == 0) {
+  auto mma_s = [&](int hf) {
     tc::fence_after_sync();
-    // S = Q K^T: K = head_dim in steps of 16 (256 bytes of each tile)
 #pragma unroll 1
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint64_t a = tc::smem_desc(sb + OFF_Q + 256 * ks, 128, (D / 8) * 128);
-      tc::mma_f16(tmem + D, a, tc::smem_desc(sb + OFF_KHI + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
+      tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
       if constexpr (kKLo)
-        tc::mma_f16(tmem + D, a, tc::smem_desc(sb + OFF_KLO + 256 * ks, 128, (D / 8) * 128), idesc_s, 1);
+        tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + KHB + 256 * ks, 128, (D / 8) * 128), idesc_s,
+                    1);
     }
     tc::commit(bar_s);
-  }
-
-  // V^T tiles (dim rows, tokens along K) while the score MMAs run.  A task is
-  // one staged page half (8 tokens) and a group of dims; it writes one 16-byte
-  // row of a core matrix per dim: dim dd, token group g at
-  // ((dd/8) * NC/8 + g) * 128 + (dd%8) * 16.  Loads first.
-  auto vt_store = [&](int dd, int g, uint4 h, uint4 l) {
-    const uint32_t off = ((dd >> 3) * (NC / 8) + g) * 128 + (dd & 7) * 16;
-    sts128(sb + OFF_VHI + off, h);
-    if constexpr (kVLo) sts128(sb + OFF_VLO + off, l);
   };
-  if constexpr (VF == MEMRA_KV_NVFP4) {
-    // task (page, half, 16-dim block b16, rr): dims 16 b16 + rr and + 8
-    uint32_t cw[VIT][4], sw[VIT][4];
-#pragma unroll
-    for (int it = 0; it < VIT; ++it) {
-      const int task = tid + it * kThreads;
-      const int rr = task & 7, b16 = (task >> 3) % (D / 16), ps = task / (16 * (D / 16));
-      const uint32_t seg = sb + OFF_RAWV + ps * VSEG;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        cw[it][c] = lds32(seg + ((b16 >> 2) * 32 + 4 * rr + c) * 16 + (b16 & 3) * 4);
-        sw[it][c] = lds32(seg + 8 * D + (c * (D / 16) + b16) * 4);
-      }
+  // O (+)= P[:, half hf] V^T (K = the half's tokens in steps of 16)
+  auto mma_o = [&](int hf) {
+    tc::fence_after_sync();
+#pragma unroll 1
+    for (int ks = 0; ks < H / 16; ++ks) {
+      const uint64_t a = tc::smem_desc(sb + OFF_K + 256 * (hf * (H / 16) + ks), 128, (NC / 8) * 128);
+      tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_V + 256 * ks, 128, (H / 8) * 128), idesc_o, hf > 0 || ks > 0);
+      if constexpr (kVLo)
+        tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_V + VHB + 256 * ks, 128, (H / 8) * 128), idesc_o, 1);
     }
-#pragma unroll
-    for (int it = 0; it < VIT; ++it) {
-      const int task = tid + it * kThreads;
-      const int rr = task & 7, b16 = (task >> 3) % (D / 16), ph = (task / (8 * (D / 16))) & 1,
-                ps = task / (16 * (D / 16));
-      uint32_t h0[4] = {0, 0, 0, 0}, h1[4] = {0, 0, 0, 0};
-      if (ok && ((pmask >> ps) & 1u)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          __half2 v[2];
-#pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            const int sh = 8 * (f + 2 * ph);
-            v[f] = __hmul2(bits_h2(e2m1x2_to_half2((cw[it][c] >> sh) & 0xFFu)), e4m3_scale_h2(sw[it][c] >> sh));
-          }
-          h0[c] = h2_bits(__lows2half2(v[0], v[1]));
-          h1[c] = h2_bits(__highs2half2(v[0], v[1]));
-        }
-      }
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      vt_store(16 * b16 + rr, 2 * ps + ph, make_uint4(h0[0], h0[1], h0[2], h0[3]), z);
-      vt_store(16 * b16 + rr + 8, 2 * ps + ph, make_uint4(h1[0], h1[1], h1[2], h1[3]), z);
-    }
-  } else {
-    // task (page, half, block b, vg): dims 32 b + 4 vg + (2 h + s), tokens 8 half + 2 c + f
-    VRaw vr[VIT];
-#pragma unroll
-    for (int it = 0; it < VIT; ++it) {
-      const int task = tid + it * kThreads;
-      const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, ps = task / (16 * NB);
-      vr[it] = load_v_task<D, VF>(sb + OFF_RAWV + ps * VSEG, ph, b, vg);
-    }
-#pragma unroll
-    for (int it = 0; it < VIT; ++it) {
-      const int task = tid + it * kThreads;
-      const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, ps = task / (16 * NB);
-      uint32_t hi[4][4], lo[4][4];
-      convert_v_task<VF>(vr[it], ph, b, hi, lo);
-      const bool have = ok && ((pmask >> ps) & 1u);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint4 h = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
-        const uint4 l = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
-        vt_store(32 * b + 4 * vg + e, 2 * ps + ph, h, l);
-      }
-    }
-  }
-  fence_proxy_async();
-  __syncthreads();                 // the raw pages are free: the softmax exchange goes there
+    tc::commit(bar_o);
+  };
+  auto sync_tiles = [&]() {        // thread-written tiles -> the tensor cores (uniform result)
+    fence_proxy_async();
+    tc::fence_before_sync();
+    ok = !__syncthreads_or(!ok);
+  };
+
+  // first half of K, its scores; the first half of V meanwhile
+  stage_k(0);
+  sync_tiles();
+  if (ok && tid == 0) mma_s(0);
+  stage_v(0);
+  // second half of K once the first half's MMAs have read the buffer
+  if (ok) ok = mbar_wait_bounded(bar_s, 0, p.status);
+  stage_k(1);
+  sync_tiles();
+  if (ok && tid == 0) mma_s(1);
 
   // Softmax of each row: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
   // (rows), columns half (w / 4) of the chunk.
   const int quarter = warp & 3, colh = warp >> 2;
   const int rl = quarter * 32 + lane;
   const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
-  float *xm = reinterpret_cast<float *>(smem + OFF_RAWK);           // [2][128] row maxima
-  float *xl = xm + 2 * kTileRows;                                     // [2][128] row sums
   constexpr int HC = NC / 2;
   float m_row = -INFINITY, l_row = 0.f;
-  if (ok) ok = mbar_wait_bounded(bar_s, 0, p.status);
+  if (ok) ok = mbar_wait_bounded(bar_s, 1, p.status);
   ok = !__syncthreads_or(!ok);
   if (ok) {
     tc::fence_after_sync();
@@ -469,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
     xm[colh * kTileRows + rl] = mloc;
     __syncthreads();
     m_row = fmaxf(xm[rl], xm[kTileRows + rl]);
-    // P (fp16) over K^ hi: row rl, token group g at ((rl/8) * NC/8 + g) * 128 + (rl%8) * 16
+    // P (fp16) over the K buffer: row rl, token group g at ((rl/8) * NC/8 + g) * 128 + (rl%8) * 16
     float lsum = 0.f;
 #pragma unroll
     for (int g = 0; g < HC / 8; ++g) {
@@ -484,33 +550,25 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
         w4[e] = h2_bits(ph2);
       }
       const int gg = colh * (HC / 8) + g;
-      sts128(sb + OFF_KHI + ((rl >> 3) * (NC / 8) + gg) * 128 + (rl & 7) * 16, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+      sts128(sb + OFF_K + ((rl >> 3) * (NC / 8) + gg) * 128 + (rl & 7) * 16, make_uint4(w4[0], w4[1], w4[2], w4[3]));
     }
     xl[colh * kTileRows + rl] = lsum;
-    fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    l_row = xl[rl] + xl[kTileRows + rl];
-    if (tid == 0) {
-      tc::fence_after_sync();
-      // O = P V: K = chunk tokens in steps of 16
-#pragma unroll 1
-      for (int ks = 0; ks < NC / 16; ++ks) {
-        const uint64_t a = tc::smem_desc(sb + OFF_KHI + 256 * ks, 128, (NC / 8) * 128);
-        tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_VHI + 256 * ks, 128, (NC / 8) * 128), idesc_o, ks > 0);
-        if constexpr (kVLo)
-          tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_VLO + 256 * ks, 128, (NC / 8) * 128), idesc_o, 1);
-      }
-      tc::commit(bar_o);
-    }
-    ok = mbar_wait_bounded(bar_o, 0, p.status);
   }
+  sync_tiles();
+  if (ok) l_row = xl[rl] + xl[kTileRows + rl];
+  if (ok && tid == 0) mma_o(0);
+  // second half of V once the first half's MMAs have read the buffer
+  if (ok) ok = mbar_wait_bounded(bar_o, 0, p.status);
+  stage_v(1);
+  sync_tiles();
+  if (ok && tid == 0) mma_o(1);
+  if (ok) ok = mbar_wait_bounded(bar_o, 1, p.status);
   ok = !__syncthreads_or(!ok);
 
   if (ok) {
     tc::fence_after_sync();
     // o = O * v_post / l into padded shared-memory rows (Q, K^, P and V^T are
-    // no longer read), then whole rows to the workspace with coalesced stores
+    // no longer read)
     const float inv = l_row > 0.f ? p.v_post / l_row : 0.f;
 #pragma unroll 1
     for (int k0 = 0; k0 < D / 2; k0 += 32) {
@@ -527,21 +585,59 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Casca
                           __float_as_uint(__uint_as_float(orr[e + 2]) * inv),
                           __float_as_uint(__uint_as_float(orr[e + 3]) * inv)));
     }
-    if (colh == 0 && r0 + rl < rows) {
-      const int r = r0 + rl, b = r / rows_per_seq, rem = r % rows_per_seq;
-      const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
-                           rem % p.group;
-      p.lse_pre[rowid * p.n_chunks + chunk] = l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
-    }
-    __syncthreads();
-    for (int lr = warp; lr < kTileRows && r0 + lr < rows; lr += kThreads / 32) {
-      const int r = r0 + lr, b = r / rows_per_seq, rem = r % rows_per_seq;
-      const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
-                           rem % p.group;
-      float4 *dst = reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_chunks + chunk) * D);
-      for (int j = lane; j < D / 4; j += 32) dst[j] = *reinterpret_cast<const float4 *>(smem + OFF_Q + lr * ROWB + 16 * j);
-    }
   }
+  if (colh == 0) xlse[rl] = ok && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
+
+  // The CTAs of a cluster hold consecutive chunks of the same rows: CTA rank
+  // c merges rows c * 128/CL .. of every CTA's shared memory (log-sum-exp) and
+  // writes one partial per row for the cluster's chunks, with coalesced
+  // stores.  The second cluster barrier keeps each CTA's rows in place until
+  // its peers have read them.
+  const int CL = p.cluster;
+  const uint32_t crank = cluster_ctarank();
+  const int part = chunk / CL;
+  const int rpc = kTileRows / CL;
+  cluster_sync();
+  for (int lr = static_cast<int>(crank) * rpc + warp; lr < (static_cast<int>(crank) + 1) * rpc; lr += kThreads / 32) {
+    const int r = r0 + lr;
+    if (r >= rows) break;
+    float lsk[8];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lsk[k] = k < CL ? ld_peer_f32(map_peer(smem_addr(xlse + lr), k)) : -INFINITY;
+      M = fmaxf(M, lsk[k]);
+    }
+    float4 acc[D / 128];
+#pragma unroll
+    for (int q = 0; q < D / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = lsk[k] == -INFINITY ? 0.f : fast_exp2(lsk[k] - M);
+      if (w == 0.f) continue;              // no key there (or a peer that gave up): never read
+      L += w;
+      const uint32_t row = map_peer(sb + OFF_Q + lr * ROWB, k);
+#pragma unroll
+      for (int q = 0; q < D / 128; ++q) {
+        const float4 x = ld_peer_v4(row + 16 * (lane + 32 * q));
+        acc[q].x = fmaf(w, x.x, acc[q].x);
+        acc[q].y = fmaf(w, x.y, acc[q].y);
+        acc[q].z = fmaf(w, x.z, acc[q].z);
+        acc[q].w = fmaf(w, x.w, acc[q].w);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int b = r / rows_per_seq, rem = r % rows_per_seq;
+    const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                         rem % p.group;
+    float4 *dst = reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_parts + part) * D);
+#pragma unroll
+    for (int q = 0; q < D / 128; ++q)
+      dst[lane + 32 * q] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    if (lane == 0) p.lse_pre[rowid * p.n_parts + part] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  }
+  cluster_sync();
 
   // Every sequence of the row tile must hold the same prefix pages and see all
   // of the prefix (flags only, off the critical path; one KV head checks).
@@ -574,14 +670,14 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
   const int b = row / (p.q_len * p.n_heads), qi = (row / p.n_heads) % p.q_len;
   const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, false, p.status, false);
   const int ns = min(key_range(Tseq, p.q_len, qi, 0, p.prefix_len, p.split_target).ns, p.nsplit_max);
-  const int parts = p.n_chunks + ns;
+  const int parts = p.n_parts + ns;
   auto lse_of = [&](int k) {
-    return k < p.n_chunks ? p.lse_pre[static_cast<size_t>(row) * p.n_chunks + k]
-                          : p.lse_suf[static_cast<size_t>(row) * p.nsplit_max + (k - p.n_chunks)];
+    return k < p.n_parts ? p.lse_pre[static_cast<size_t>(row) * p.n_parts + k]
+                         : p.lse_suf[static_cast<size_t>(row) * p.nsplit_max + (k - p.n_parts)];
   };
   auto o_of = [&](int k) {
-    return k < p.n_chunks ? p.o_pre + (static_cast<size_t>(row) * p.n_chunks + k) * D
-                          : p.o_suf + (static_cast<size_t>(row) * p.nsplit_max + (k - p.n_chunks)) * D;
+    return k < p.n_parts ? p.o_pre + (static_cast<size_t>(row) * p.n_parts + k) * D
+                         : p.o_suf + (static_cast<size_t>(row) * p.nsplit_max + (k - p.n_parts)) * D;
   };
   float m = -INFINITY;
   for (int k = threadIdx.x; k < parts; k += kThreads) m = fmaxf(m, lse_of(k));
@@ -644,23 +740,75 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
 }
 
 template <int D, int KF, int VF>
-cudaError_t launch_prefix_one(const CascadeParams &p, cudaStream_t st) {
+cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   constexpr uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D));
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(cascade_prefix_kernel<D, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  auto kernel = cascade_prefix_kernel<D, KF, VF>;
+  // Cluster size, per device and instantiation: the largest of 8, 4, 2 whose
+  // co-resident clusters still cover 90% of the CTA slots (on 152 SMs,
+  // clusters of 8 CTAs of 197 KB fit only 15 at a time), else 1.
+  // It depends on the device and the formats only, never on the batch.
+  static int widest[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!widest[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int slots = sms * (per_sm > 0 ? per_sm : 1);
+    int w = 1;
+    for (int cl = 8; cl > 1; cl /= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && 10 * n * cl >= 9 * slots) {
+        w = cl;
+        break;
+      }
+      cudaGetLastError();    // a refused query is not an error of this call
+    }
+    widest[dev] = w;
   }
+  int cl = widest[dev];
+  while (cl > 1 && cl > p.n_chunks) cl /= 2;
+  p.cluster = cl;
+  p.n_parts = (p.n_chunks + cl - 1) / cl;
   const int rows = p.batch * p.q_len * p.group;
-  const dim3 grid(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.n_kv_heads),
-                  static_cast<unsigned>((rows + kTileRows - 1) / kTileRows));
-  return launch_pdl(cascade_prefix_kernel<D, KF, VF>, grid, dim3(kThreads), smem, st, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_parts * cl), static_cast<unsigned>(p.n_kv_heads),
+                     static_cast<unsigned>((rows + kTileRows - 1) / kTileRows));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const CascadeParams args = p;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 template <int D>
-cudaError_t prefix_formats(int kf, int vf, const CascadeParams &p, cudaStream_t st) {
+cudaError_t prefix_formats(int kf, int vf, CascadeParams &p, cudaStream_t st) {
   auto by_v = [&](auto kc) -> cudaError_t {
     constexpr int K = decltype(kc)::value;
     switch (vf) {
@@ -681,7 +829,7 @@ cudaError_t prefix_formats(int kf, int vf, const CascadeParams &p, cudaStream_t 
 
 }  // namespace
 
-cudaError_t launch_cascade_prefix(int D, int kf, int vf, const CascadeParams &p, cudaStream_t st) {
+cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st) {
   if (p.n_chunks == 0 || p.batch == 0) return cudaSuccess;
   return D == 128 ? prefix_formats<128>(kf, vf, p, st) : prefix_formats<256>(kf, vf, p, st);
 }

@@ -12,8 +12,10 @@
 
 namespace memra {
 
-// Prefix tokens one CTA of the prefix pass covers (the N of its score MMA).
-__host__ __device__ constexpr int cascade_chunk_tokens(int D) { return D == 128 ? 128 : 64; }
+// Prefix tokens one CTA of the prefix pass covers (the N of its score MMA),
+// and its CTAs per SM (registers and shared memory allow two at head_dim 128).
+__host__ __device__ constexpr int cascade_chunk_tokens(int D) { return D == 128 ? 64 : 64; }
+__host__ __device__ constexpr int cascade_ctas_per_sm(int D) { return D == 128 ? 2 : 1; }
 
 struct CascadeParams {
   const uint8_t *k_pool;
@@ -22,9 +24,11 @@ struct CascadeParams {
   const int32_t *page_table;
   const int32_t *seq_lens;
   int32_t *status;
-  float *o_pre;       // [batch * q_len * n_heads][n_chunks][D], row id (b * q_len + i) * n_heads + h
-  float *lse_pre;     // [batch * q_len * n_heads][n_chunks]
+  float *o_pre;       // [batch * q_len * n_heads][n_parts][D], row id (b * q_len + i) * n_heads + h
+  float *lse_pre;     // [batch * q_len * n_heads][n_parts]
   int batch, q_len, n_heads, group, n_kv_heads, num_pages, max_pages, prefix_len, n_chunks;
+  int cluster;        // CTAs per cluster along the chunks (1, 2, 4 or 8), set by the launcher
+  int n_parts;        // prefix partials per row: ceil(n_chunks / cluster), set by the launcher
   float scale_log2;   // sm_scale * (post-scale of the staged K values) * log2(e)
   float v_post;       // post-scale of the staged V values
 };
@@ -37,16 +41,19 @@ struct CascadeCombineParams {
   const float *lse_suf;
   __half *out;
   int32_t *status;
-  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max, split_target, prefix_len, n_chunks;
+  int rows, q_len, n_heads, max_seq_len, max_pages, nsplit_max, split_target, prefix_len;
+  int n_parts;            // prefix partials per row (CascadeParams::n_parts of the prefix pass)
 };
 
 // Shared memory of one prefix-pass CTA for head_dim D and the formats' segment bytes.
 __host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg) {
-  return 128u * D * 2 + 4u * cascade_chunk_tokens(D) * D * 2 +
+  return 128u * D * 2 + 2u * cascade_chunk_tokens(D) * D * 2 +
          static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 64u;
 }
 
-cudaError_t launch_cascade_prefix(int D, int kf, int vf, const CascadeParams &p, cudaStream_t st);
+// Chooses the cluster size (the largest of 8, 4, 2, 1 not above n_chunks that
+// the device can co-schedule), fills p.cluster and p.n_parts, and launches.
+cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st);
 cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st);
 
 }  // namespace memra

@@ -138,7 +138,7 @@ __device__ __forceinline__ KeyRange key_range(int Tseq, int q_len, int qi, int w
   k.lo = max(k.lo, 0);
   k.base = k.lo & ~(kPage - 1);
   const int L = k.T - k.base;
-  k.C = split_tokens(L, split_target);
+  k.C = split_tokens(L, split_target, skip > 0 ? kCascadeSplitTokens : kSplitTokens);
   k.ns = k.T > 0 && L > 0 ? (L + k.C - 1) / k.C : 0;
   return k;
 }
@@ -192,7 +192,12 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
     for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
     fence_barrier_init();
   }
-  grid_dependency_wait();       // inputs written by the launch before this one have landed
+  // Inputs written by the launch before this one have landed.  A cascade
+  // call's own-key pass (skip > 0) runs beside the prefix pass launched just
+  // before it instead: it reads nothing that pass writes, and the call's
+  // inputs were complete before that pass let it start.  It waits for that
+  // pass at its end, so that the merge after it sees both.
+  if (p.skip == 0) grid_dependency_wait();
 
   // This CTA: query position qi of sequence b and query heads 8 hg .. 8 hg + 7
   // of KV head kvh's group, over the keys visible to position qi (the first
@@ -836,6 +841,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       if (j4 == 0) p.lse_part[pidx] = L > 0.f ? M + __log2f(L) : -INFINITY;
     }
   }
+  if (p.skip != 0) grid_dependency_wait();
   allow_dependent_launch();
 }
 

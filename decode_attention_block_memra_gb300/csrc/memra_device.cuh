@@ -16,15 +16,19 @@ constexpr int kPage = MEMRA_PAGE_SIZE;
 constexpr int kSplitTokens = MEMRA_SPLIT_TOKENS;            // smallest split
 constexpr int kSplitTokensMax = MEMRA_SPLIT_TOKENS_MAX;      // largest split
 constexpr int kSplitPagesMax = kSplitTokensMax / kPage;
+// Smallest split of a cascade call's own keys (the part after the shared
+// prefix): short, so that the few own keys of many sequences spread over the GPU.
+constexpr int kCascadeSplitTokens = 256;
 
-// Split size of a sequence of T tokens: enough splits to give one long
-// sequence `target` CTAs per KV head, never below 1024 or above 8192 tokens,
-// a multiple of the page.  Depends on T and the device only.
-__host__ __device__ __forceinline__ int split_tokens(int T, int target) {
+// Split size of a range of T tokens: enough splits to give one long sequence
+// `target` CTAs per KV head, never below `min_tokens` (1024; 256 for a cascade
+// call's own keys) or above 8192 tokens, a multiple of the page.  Depends on T
+// and the device only.
+__host__ __device__ __forceinline__ int split_tokens(int T, int target, int min_tokens) {
   const int t = target > 0 ? target : 1;
   int c = (T + t - 1) / t;
   c = (c + kPage - 1) / kPage * kPage;
-  return c < kSplitTokens ? kSplitTokens : (c > kSplitTokensMax ? kSplitTokensMax : c);
+  return c < min_tokens ? min_tokens : (c > kSplitTokensMax ? kSplitTokensMax : c);
 }
 
 // Segment bytes per (format, side, head_dim); see the layout in memra.h.
