@@ -64,7 +64,7 @@ def test_cascade_formats(kf, vf, D):
 
 @pytest.mark.parametrize("q_len", [1, 4])
 def test_cascade_fused_step_pools_and_rows(q_len):
-    # prefix 1,040 = 8 chunks of 128 and one of 16 tokens; the step's rows are stored by the split kernel
+    # prefix 1,040 = 16 chunks of 64 and one of 16 tokens; the step's rows are stored by the split kernel
     w = small(q_len=q_len, prefix=1040, seq_lens=(1100, 1044, 2090, 1300), seed=32)
     res = run(w, fused=True, want_pools=True)
     assert res.flags == 0
@@ -190,3 +190,17 @@ def test_cascade_host_validation():
     assert memra.read_status(dw.cache) == 0
     assert call(0) == 0                         # the plain call
     assert memra.read_status(dw.cache) == 0
+
+
+@pytest.mark.parametrize("case", ["one_page_prefix", "ten_row_tiles", "d256_ragged"])
+def test_cascade_edges(case):
+    if case == "one_page_prefix":          # one chunk, no cluster partner
+        w = small(prefix=16, seq_lens=(17, 40, 300), seed=38)
+    elif case == "ten_row_tiles":          # 40 sequences x q_len 4 x group 8 = 1,280 rows per KV head
+        lens = [400 + 29 * i for i in range(40)]
+        w = small(q_len=4, prefix=384, seq_lens=lens, seed=39)
+    else:                                  # head_dim 256, own keys from 1 to 2,000 tokens, verify rows
+        w = small(D=256, q_len=2, prefix=832, seq_lens=(834, 1000, 2832, 900), seed=40, kf="fp8", vf="q4_0")
+    res = run(w, fused=True)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
