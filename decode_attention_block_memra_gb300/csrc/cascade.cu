@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
                      OFF_RAWV = OFF_RAWK + NPG * KSEG, OFF_BAR = OFF_RAWV + NPG * VSEG;
   constexpr uint32_t OFF_X = OFF_RAWV - 5 * kTileRows * 4;    // [2][128] max, [2][128] sum, [128] lse
   constexpr uint32_t ROWB = D * 4 + 16;                       // padded output row in shared memory
-  constexpr uint32_t TCOLS = D + NC <= 256 ? 256 : 512;       // O at column 0, S at column D
+  constexpr uint32_t TCOLS = cascade_tmem_cols(D);            // O at column 0; S there too until read
   static_assert(OFF_BAR + 64 == cascade_smem_bytes(D, KSEG, VSEG), "shared-memory plan");
   static_assert(OFF_BAR + 64 <= kSmemLimit, "shared memory");
   static_assert(OFF_X >= OFF_RAWK && kTileRows * ROWB <= OFF_X, "output rows below the exchange");
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     }
   };
   // S[:, half hf] = Q K^T (N = H tokens, K = head_dim in steps of 16), into
-  // tensor-memory columns D + hf * H ..
+  // tensor-memory columns hf * H .. (the first O MMA overwrites them later)
   constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, H);
   constexpr uint32_t idesc_o = tc::idesc_f16_f32(kTileRows, D);
   auto mma_s = [&](int hf) {
@@ -472,10 +472,9 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
 #pragma unroll 1
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint64_t a = tc::smem_desc(sb + OFF_Q + 256 * ks, 128, (D / 8) * 128);
-      tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
+      tc::mma_f16(tmem + hf * H, a, tc::smem_desc(sb + OFF_K + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
       if constexpr (kKLo)
-        tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + KHB + 256 * ks, 128, (D / 8) * 128), idesc_s,
-                    1);
+        tc::mma_f16(tmem + hf * H, a, tc::smem_desc(sb + OFF_K + KHB + 256 * ks, 128, (D / 8) * 128), idesc_s, 1);
     }
     tc::commit(bar_s);
   };
@@ -521,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     tc::fence_after_sync();
     uint32_t sr[HC];
 #pragma unroll
-    for (int k0 = 0; k0 < HC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + D + colh * HC + k0, sr + k0);
+    for (int k0 = 0; k0 < HC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + colh * HC + k0, sr + k0);
 #pragma unroll
     for (int k0 = 0; k0 < HC; k0 += 16) tc::wait_ld(sr + k0);
     float mloc = -INFINITY;
@@ -742,6 +741,12 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
 template <int D, int KF, int VF>
 cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   constexpr uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D));
+  // any mix of prefix-pass CTAs that fits an SM by shared memory fits its tensor memory
+  constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128) + 1024u;   // smallest CTAs
+  constexpr uint32_t kMin256 = cascade_smem_bytes(256, 9 * 256, 9 * 256) + 1024u;
+  static_assert(4u * kMin128 > 233472u && 3u * cascade_tmem_cols(128) <= 512u, "three 128s at most");
+  static_assert(2u * kMin256 > 233472u && kMin256 + 2u * kMin128 > 233472u &&
+                    cascade_tmem_cols(256) + cascade_tmem_cols(128) <= 512u, "one 256 and one 128 at most");
   auto kernel = cascade_prefix_kernel<D, KF, VF>;
   // Cluster size, per device and instantiation: the largest of 8, 4, 2 whose
   // co-resident clusters still cover 90% of the CTA slots (on 152 SMs,

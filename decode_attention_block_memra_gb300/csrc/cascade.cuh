@@ -51,6 +51,16 @@ __host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int v
          static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 64u;
 }
 
+// Tensor-memory columns of one prefix-pass CTA: the O accumulator's head_dim
+// columns, which also hold the chunk's scores S until the softmax has read
+// them (the first O MMA overwrites them).  The hardware places CTAs, and whole
+// clusters, by registers and shared memory, not by tensor memory, so any mix
+// of prefix-pass CTAs that fits an SM by shared memory must fit its 512
+// columns: at most three of head_dim 128 (>= 74 KB each, 384 columns) or one
+// of each head_dim (384 columns).  A CTA that found the columns taken would
+// wait in its allocation while its cluster peers wait for it.
+__host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) { return static_cast<uint32_t>(D); }
+
 // Chooses the cluster size (the largest of 8, 4, 2, 1 not above n_chunks that
 // the device can co-schedule), fills p.cluster and p.n_parts, and launches.
 cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st);
