@@ -92,7 +92,8 @@ int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan
   const size_t qbytes = static_cast<size_t>(W) * (D / 32) * 512;     // warp-private Q fragments
   size_t cta = (226 * 1024) / ctas_per_sm;
   if (max_cta_smem && max_cta_smem < cta) cta = max_cta_smem;
-  const size_t budget = cta - 2048 - qbytes - 4 * static_cast<size_t>(kSplitPagesMax);
+  const size_t fixed = 2048 + qbytes + 4 * static_cast<size_t>(kSplitPagesMax);
+  const size_t budget = cta > fixed ? cta - fixed : 0;     // below the smallest plan: W stages anyway
   int ns = static_cast<int>(budget / stage) & ~(W - 1);
   if (ns > 32) ns = 32;
   if (ns < W) ns = W;
@@ -197,6 +198,16 @@ int check_decode(const DecodeArgs &a) {
   return MEMRA_OK;
 }
 
+// Chunks per prefix-pass CTA of a cascade call: enough CTAs per KV head for
+// one wave of one row tile, never more than kCascadeMaxChunksPerCta chunks
+// each.  Depends on the prefix, head_dim, KV heads and the device only.
+int cascade_cpc(int32_t prefix, int32_t head_dim, int32_t n_kv_heads) {
+  const int64_t n_chunks = ceil_div(prefix, cascade_chunk_tokens(head_dim));
+  const int64_t target = std::max<int64_t>(1, device_sms() * cascade_ctas_per_sm(head_dim) / n_kv_heads);
+  return static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(n_chunks, target), 1),
+                                            kCascadeMaxChunksPerCta));
+}
+
 // k_new / v_new: the fused append's rows, or null for attention alone.
 int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cudaStream_t st) {
   const memra_kv_cache &c = *a.cache;
@@ -207,7 +218,8 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   const size_t cap = a.prefix > 0 ? kSmPerSm - kSmReservedPerCta * (1 + pre_per_sm) -
                                         pre_per_sm * static_cast<size_t>(cascade_smem_bytes(
                                                          a.head_dim, k_seg_bytes(c.k_fmt, a.head_dim),
-                                                         v_seg_bytes(c.v_fmt, a.head_dim)))
+                                                         v_seg_bytes(c.v_fmt, a.head_dim),
+                                                         cascade_cpc(a.prefix, a.head_dim, a.n_kv_heads)))
                                   : 0;
   int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl, cap);
   if (rc) return rc;
@@ -406,6 +418,7 @@ int cascade_passes(const DecodeArgs &a, const void *k_new, const void *v_new, vo
   cp.max_pages = a.max_pages_per_seq;
   cp.prefix_len = a.prefix;
   cp.n_chunks = n_chunks;
+  cp.cpc = cascade_cpc(a.prefix, a.head_dim, a.n_kv_heads);
   // staged values: q8_0 / q5_1 / q4_0 at half size, fp8 / NVFP4 without their tensor scale
   const float k_post = c.k_fmt == MEMRA_KV_Q8_0 ? 2.f : c.k_scale;
   cp.scale_log2 = a.sm_scale * k_post * 1.4426950408889634f;

@@ -244,7 +244,7 @@ __device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, uin
 
 template <int D, int KF, int VF>
 __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_prefix_kernel(const CascadeParams p) {
-  constexpr int NC = cascade_chunk_tokens(D);       // prefix tokens of this CTA
+  constexpr int NC = cascade_chunk_tokens(D);       // prefix tokens of one chunk
   constexpr int H = NC / 2;                         // tokens staged at a time (one half)
   constexpr int NPG = NC / kPage;
   constexpr int HPG = H / kPage;                    // pages of a half
@@ -253,23 +253,32 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   constexpr int VSEG = v_seg_bytes(VF, D);
   constexpr bool kKLo = KF == MEMRA_KV_Q8_0;
   constexpr bool kVLo = VF == MEMRA_KV_Q5_1 || VF == MEMRA_KV_Q4_0;
+  constexpr float kLazy = 8.f;                      // log2 units: P stays <= 256 between rescales
   // Shared memory (byte offsets): the Q tile; one half of K^ (hi, lo; token
-  // rows) and P after the scores; one half of V^T (hi, lo; dim rows); the raw
-  // pages of the chunk (K, then V); barriers.  The softmax exchange and the
-  // row lse sit at the end of the raw K pages, which are dead once the second
-  // half of K is staged (the raw V pages are read until the end); the output
-  // rows reuse Q, K^ and V^T once O is done.
+  // rows) and P after the scores; one half of V^T (hi, lo; dim rows); two
+  // buffers of raw pages (a chunk's K pages, then its V pages), the next
+  // chunk's copies landing in one while the other is staged; the softmax
+  // exchange and row lse; the page ids of the CTA's chunks; barriers.  The
+  // output rows reuse Q, K^, V^T and the raw buffers once O is done.
   constexpr uint32_t QB = kTileRows * D * 2, KHB = H * D * 2, VHB = D * H * 2;
-  constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 2 * KHB, OFF_RAWK = OFF_V + 2 * VHB,
-                     OFF_RAWV = OFF_RAWK + NPG * KSEG, OFF_BAR = OFF_RAWV + NPG * VSEG;
-  constexpr uint32_t OFF_X = OFF_RAWV - 5 * kTileRows * 4;    // [2][128] max, [2][128] sum, [128] lse
+  constexpr uint32_t RAWB = NPG * (KSEG + VSEG);
+  constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 2 * KHB, OFF_RAW = OFF_V + 2 * VHB;
   constexpr uint32_t ROWB = D * 4 + 16;                       // padded output row in shared memory
-  constexpr uint32_t TCOLS = cascade_tmem_cols(D);            // O at column 0; S there too until read
-  static_assert(OFF_BAR + 64 == cascade_smem_bytes(D, KSEG, VSEG), "shared-memory plan");
-  static_assert(OFF_BAR + 64 <= kSmemLimit, "shared memory");
-  static_assert(OFF_X >= OFF_RAWK && kTileRows * ROWB <= OFF_X, "output rows below the exchange");
+  constexpr uint32_t TCOLS = cascade_tmem_cols(D);            // O at column 0, S at column D
+  // one raw buffer when the CTA has one chunk, two when it loops over several
+  const uint32_t nbuf = p.cpc > 1 ? 2u : 1u;
+  const uint32_t OFF_X = OFF_RAW + nbuf * RAWB, OFF_PID = OFF_X + 5 * kTileRows * 4,
+                 OFF_BAR = OFF_PID + 4 * NPG * p.cpc;
+  static_assert(OFF_RAW + 2 * RAWB + 5 * kTileRows * 4 + 4 * NPG * kCascadeMaxChunksPerCta + 64 ==
+                    cascade_smem_plan(D, KSEG, VSEG, kCascadeMaxChunksPerCta) &&
+                    OFF_RAW + RAWB + 5 * kTileRows * 4 + 4 * NPG + 64 == cascade_smem_plan(D, KSEG, VSEG, 1),
+                "shared-memory plan");
+  static_assert(cascade_smem_bytes(D, KSEG, VSEG, kCascadeMaxChunksPerCta) <= kSmemLimit, "shared memory");
+  static_assert(kTileRows * ROWB <= OFF_RAW + RAWB, "output rows below the exchange");
   static_assert(kTileRows * NC * 2 <= 2 * KHB, "P fits the K^ half");
-  static_assert(KSEG % 16 == 0 && VSEG % 16 == 0 && OFF_RAWK % 16 == 0 && OFF_BAR % 16 == 0, "alignment");
+  static_assert(D + NC <= static_cast<int>(TCOLS), "O and S fit the tensor memory");
+  static_assert(KSEG % 16 == 0 && VSEG % 16 == 0 && OFF_RAW % 16 == 0 && RAWB % 16 == 0 && (4 * NPG) % 16 == 0,
+                "alignment");
   constexpr int QIT = kTileRows * (D / 8) / kThreads;        // Q items per thread
   constexpr int KIT = H * (D / 8) / kThreads;                // K items per thread and half
   constexpr int VTASKS = VF == MEMRA_KV_NVFP4 ? HPG * 2 * (D / 16) * 8 : HPG * 2 * NB * 8;
@@ -280,18 +289,18 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t bar_raw = sb + OFF_BAR, bar_s = bar_raw + 8, bar_o = bar_raw + 16;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 24);
-  int *pid_s = reinterpret_cast<int *>(smem + OFF_BAR + 32);      // NPG <= 8 page ids
+  const uint32_t bar_raw0 = sb + OFF_BAR, bar_s = bar_raw0 + 16, bar_o = bar_raw0 + 24;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 32);
+  int *pid_s = reinterpret_cast<int *>(smem + OFF_PID);        // [chunk of the CTA][page], -1 = none
   float *xm = reinterpret_cast<float *>(smem + OFF_X);
   float *xl = xm + 2 * kTileRows;
   float *xlse = xl + 2 * kTileRows;
 
-  const int chunk = blockIdx.x, kvh = blockIdx.y;
+  const int kvh = blockIdx.y;
   const int rows = p.batch * p.q_len * p.group;                  // query rows of one KV head
   const int r0 = blockIdx.z * kTileRows;
-  const int tok0 = chunk * NC;
-  const int npg = min(NPG, (p.prefix_len - tok0) / kPage);       // pages of the prefix in this chunk
+  const int c0 = blockIdx.x * p.cpc;                             // this CTA's chunks: c0 .. c0 + nck - 1
+  const int nck = max(0, min(p.cpc, p.n_chunks - c0));
   const int rows_per_seq = p.q_len * p.group;
 
   if (warp == 0) {
@@ -299,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     tc::tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(bar_raw, 1);
+    mbar_init(bar_raw0, 1);
+    mbar_init(bar_raw0 + 8, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     fence_barrier_init();
@@ -307,13 +317,23 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   grid_dependency_wait();          // q, the pools and the tables are written
   allow_dependent_launch();        // the own-key split kernel may start beside this one
 
-  // This chunk's pages come from the first sequence's table.
-  int pid = -1;
-  if (tid < npg) pid = p.page_table[tok0 / kPage + tid];
+  // Page ids of all of this CTA's chunks, from the first sequence's table.
+  for (int i = tid; i < nck * NPG; i += kThreads) {
+    const int tok = c0 * NC + i * kPage;
+    int pid = -1;
+    if (tok < p.prefix_len) {
+      pid = p.page_table[tok / kPage];
+      if (pid < 0 || pid >= p.num_pages) {
+        flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+        pid = -1;
+      }
+    }
+    pid_s[i] = pid;
+  }
 
   // Q rows of the tile in core-matrix order: item i = (row group, 8-dim group,
   // row in group), shared-memory byte 16 i.  All of a thread's loads are in
-  // flight together, beside the page-id load.
+  // flight together, beside the page-id loads.
   uint4 qv[QIT];
 #pragma unroll
   for (int it = 0; it < QIT; ++it) {
@@ -328,44 +348,42 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
       qv[it] = *reinterpret_cast<const uint4 *>(p.q + rowid * D + 8 * u);
     }
   }
-  if (tid < NPG) {
-    if (tid < npg && (pid < 0 || pid >= p.num_pages)) {
-      flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
-      pid = -1;
-    }
-    pid_s[tid] = pid;
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (tid == 0) {
+  // Copies of chunk ci (of this CTA) into raw buffer ci % 2: one bulk copy per
+  // page for K and for V, or a plain arrival when the chunk has no page.
+  const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG, vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
+  auto issue = [&](int ci) {
+    const uint32_t buf = sb + OFF_RAW + (ci & 1) * RAWB, bar = bar_raw0 + 8 * (ci & 1);
     uint32_t bytes = 0;
-    for (int i = 0; i < npg; ++i) bytes += pid_s[i] >= 0 ? KSEG + VSEG : 0;
-    if (bytes) {
-      mbar_arrive_expect_tx(bar_raw, bytes);
-      const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG, vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
-      for (int i = 0; i < npg; ++i) {
-        const int pg = pid_s[i];
-        if (pg < 0) continue;
-        bulk_copy_g2s_nohint(sb + OFF_RAWK + i * KSEG, p.k_pool + pg * kstride + static_cast<size_t>(kvh) * KSEG,
-                             KSEG, bar_raw);
-        bulk_copy_g2s_nohint(sb + OFF_RAWV + i * VSEG, p.v_pool + pg * vstride + static_cast<size_t>(kvh) * VSEG,
-                             VSEG, bar_raw);
-      }
-    } else {
-      mbar_arrive(bar_raw);
+    for (int i = 0; i < NPG; ++i) bytes += pid_s[ci * NPG + i] >= 0 ? KSEG + VSEG : 0;
+    if (!bytes) {
+      mbar_arrive(bar);
+      return;
     }
+    mbar_arrive_expect_tx(bar, bytes);
+    for (int i = 0; i < NPG; ++i) {
+      const int pg = pid_s[ci * NPG + i];
+      if (pg < 0) continue;
+      bulk_copy_g2s_nohint(buf + i * KSEG, p.k_pool + pg * kstride + static_cast<size_t>(kvh) * KSEG, KSEG, bar);
+      bulk_copy_g2s_nohint(buf + NPG * KSEG + i * VSEG, p.v_pool + pg * vstride + static_cast<size_t>(kvh) * VSEG,
+                           VSEG, bar);
+    }
+  };
+  if (tid == 0) {
+    if (nck > 0) issue(0);
+    if (nck > 1) issue(1);
   }
+  int issued = min(nck, 2), consumed = 0;    // chunks whose copies were issued / waited for (all threads)
 #pragma unroll
   for (int it = 0; it < QIT; ++it) sts128(sb + OFF_Q + 16 * (tid + it * kThreads), qv[it]);
-  // pages of this chunk that hold keys, one bit each
-  uint32_t pmask = 0;
-#pragma unroll
-  for (int i = 0; i < NPG; ++i) pmask |= (i < npg && pid_s[i] >= 0 ? 1u : 0u) << i;
 
-  bool ok = mbar_wait_bounded(bar_raw, 0, p.status);
+  bool ok = true;
+  uint32_t pmask = 0;              // pages of the current chunk that hold keys, one bit each
+  uint32_t rawk = 0, rawv = 0;     // the current chunk's raw K and V pages
 
   // K^ of half hf (token rows, dims along K) at the K buffer: item i =
   // (token group, 8-dim group, token in group) at byte 16 i of hi and lo.
@@ -375,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     for (int it = 0; it < KIT; ++it) {
       const int i = tid + it * kThreads;
       const int n = hf * H + ((i >> 3) / (D / 8)) * 8 + (i & 7);
-      kr[it] = load_k8<D, KF>(sb + OFF_RAWK + (n / kPage) * KSEG, n % kPage, (i >> 3) % (D / 8));
+      kr[it] = load_k8<D, KF>(rawk + (n / kPage) * KSEG, n % kPage, (i >> 3) % (D / 8));
     }
 #pragma unroll
     for (int it = 0; it < KIT; ++it) {
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
         const int task = tid + it * kThreads;
         if (task >= VTASKS) break;
         const int rr = task & 7, b16 = (task >> 3) % (D / 16), ps = hf * HPG + task / (16 * (D / 16));
-        const uint32_t seg = sb + OFF_RAWV + ps * VSEG;
+        const uint32_t seg = rawv + ps * VSEG;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           cw[it][c] = lds32(seg + ((b16 >> 2) * 32 + 4 * rr + c) * 16 + (b16 & 3) * 4);
@@ -444,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
         if (task >= VTASKS) break;
         const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1,
                   ps = hf * HPG + task / (16 * NB);
-        vr[it] = load_v_task<D, VF>(sb + OFF_RAWV + ps * VSEG, ph, b, vg);
+        vr[it] = load_v_task<D, VF>(rawv + ps * VSEG, ph, b, vg);
       }
 #pragma unroll
       for (int it = 0; it < VIT; ++it) {
@@ -463,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
       }
     }
   };
-  // S[:, half hf] = Q K^T (N = H tokens, K = head_dim in steps of 16), into
-  // tensor-memory columns hf * H .. (the first O MMA overwrites them later)
+  // S[:, half hf] = Q K^T (N = H tokens, K = head_dim in steps of 16) into
+  // tensor-memory columns D + hf * H ..
   constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, H);
   constexpr uint32_t idesc_o = tc::idesc_f16_f32(kTileRows, D);
   auto mma_s = [&](int hf) {
@@ -472,19 +490,22 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
 #pragma unroll 1
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint64_t a = tc::smem_desc(sb + OFF_Q + 256 * ks, 128, (D / 8) * 128);
-      tc::mma_f16(tmem + hf * H, a, tc::smem_desc(sb + OFF_K + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
+      tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
       if constexpr (kKLo)
-        tc::mma_f16(tmem + hf * H, a, tc::smem_desc(sb + OFF_K + KHB + 256 * ks, 128, (D / 8) * 128), idesc_s, 1);
+        tc::mma_f16(tmem + D + hf * H, a, tc::smem_desc(sb + OFF_K + KHB + 256 * ks, 128, (D / 8) * 128), idesc_s,
+                    1);
     }
     tc::commit(bar_s);
   };
-  // O (+)= P[:, half hf] V^T (K = the half's tokens in steps of 16)
-  auto mma_o = [&](int hf) {
+  // O (+)= P[:, half hf] V^T (K = the half's tokens in steps of 16); the first
+  // MMA of the CTA's first chunk starts the accumulator
+  auto mma_o = [&](int hf, bool first_chunk) {
     tc::fence_after_sync();
 #pragma unroll 1
     for (int ks = 0; ks < H / 16; ++ks) {
       const uint64_t a = tc::smem_desc(sb + OFF_K + 256 * (hf * (H / 16) + ks), 128, (NC / 8) * 128);
-      tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_V + 256 * ks, 128, (H / 8) * 128), idesc_o, hf > 0 || ks > 0);
+      tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_V + 256 * ks, 128, (H / 8) * 128), idesc_o,
+                  !first_chunk || hf > 0 || ks > 0);
       if constexpr (kVLo)
         tc::mma_f16(tmem, a, tc::smem_desc(sb + OFF_V + VHB + 256 * ks, 128, (H / 8) * 128), idesc_o, 1);
     }
@@ -496,31 +517,46 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     ok = !__syncthreads_or(!ok);
   };
 
-  // first half of K, its scores; the first half of V meanwhile
-  stage_k(0);
-  sync_tiles();
-  if (ok && tid == 0) mma_s(0);
-  stage_v(0);
-  // second half of K once the first half's MMAs have read the buffer
-  if (ok) ok = mbar_wait_bounded(bar_s, 0, p.status);
-  stage_k(1);
-  sync_tiles();
-  if (ok && tid == 0) mma_s(1);
-
-  // Softmax of each row: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-  // (rows), columns half (w / 4) of the chunk.
+  // Online softmax over the CTA's chunks: thread (lane quarter, column half)
+  // owns row rl and half colh of the chunk's columns and of O's.  The row's
+  // reference maximum m moves only when a chunk's maximum passes it by more
+  // than kLazy; then O (in tensor memory) and l are rescaled.  Both threads of
+  // a row see the same maxima, so they take the same decisions.
   const int quarter = warp & 3, colh = warp >> 2;
   const int rl = quarter * 32 + lane;
   const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
   constexpr int HC = NC / 2;
   float m_row = -INFINITY, l_row = 0.f;
-  if (ok) ok = mbar_wait_bounded(bar_s, 1, p.status);
-  ok = !__syncthreads_or(!ok);
-  if (ok) {
+
+#pragma unroll 1
+  for (int ci = 0; ci < nck && ok; ++ci) {
+    const int b = ci & 1;
+    rawk = sb + OFF_RAW + b * RAWB;
+    rawv = rawk + NPG * KSEG;
+    pmask = 0;
+#pragma unroll
+    for (int i = 0; i < NPG; ++i) pmask |= (pid_s[ci * NPG + i] >= 0 ? 1u : 0u) << i;
+    ok = mbar_wait_bounded(bar_raw0 + 8 * b, (ci >> 1) & 1, p.status);
+
+    // first half of K, its scores; the first half of V meanwhile
+    stage_k(0);
+    sync_tiles();
+    if (ok) consumed = ci + 1;
+    if (ok && tid == 0) mma_s(0);
+    stage_v(0);
+    // second half of K once the first half's MMAs have read the buffer
+    if (ok) ok = mbar_wait_bounded(bar_s, 0, p.status);
+    stage_k(1);
+    sync_tiles();
+    if (ok && tid == 0) mma_s(1);
+    if (ok) ok = mbar_wait_bounded(bar_s, 1, p.status);
+    ok = !__syncthreads_or(!ok);
+    if (!ok) break;
+
     tc::fence_after_sync();
     uint32_t sr[HC];
 #pragma unroll
-    for (int k0 = 0; k0 < HC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + colh * HC + k0, sr + k0);
+    for (int k0 = 0; k0 < HC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + D + colh * HC + k0, sr + k0);
 #pragma unroll
     for (int k0 = 0; k0 < HC; k0 += 16) tc::wait_ld(sr + k0);
     float mloc = -INFINITY;
@@ -533,7 +569,25 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
     }
     xm[colh * kTileRows + rl] = mloc;
     __syncthreads();
-    m_row = fmaxf(xm[rl], xm[kTileRows + rl]);
+    const float m_chunk = fmaxf(xm[rl], xm[kTileRows + rl]);
+    float alpha = 1.f;
+    if (m_chunk > m_row + kLazy) {           // also the first chunk with a key (m_row = -inf)
+      if (m_row != -INFINITY) alpha = fast_exp2(m_row - m_chunk);
+      m_row = m_chunk;
+    }
+    if (ci > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // O's rows of this warp (its column half) times alpha; 1 for the rows that keep their maximum
+#pragma unroll 1
+      for (int k0 = 0; k0 < D / 2; k0 += 16) {
+        uint32_t orr[16];
+        tc::ld_32x32b_x16(tmem + tlane + colh * (D / 2) + k0, orr);
+        tc::wait_ld(orr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+        tc::st_32x32b_x16(tmem + tlane + colh * (D / 2) + k0, orr);
+      }
+      tc::wait_st();
+    }
     // P (fp16) over the K buffer: row rl, token group g at ((rl/8) * NC/8 + g) * 128 + (rl%8) * 16
     float lsum = 0.f;
 #pragma unroll
@@ -552,22 +606,26 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
       sts128(sb + OFF_K + ((rl >> 3) * (NC / 8) + gg) * 128 + (rl & 7) * 16, make_uint4(w4[0], w4[1], w4[2], w4[3]));
     }
     xl[colh * kTileRows + rl] = lsum;
+    sync_tiles();
+    l_row = l_row * alpha + (xl[rl] + xl[kTileRows + rl]);
+    if (ok && tid == 0) mma_o(0, ci == 0);
+    // second half of V once the first half's MMAs have read the buffer
+    if (ok) ok = mbar_wait_bounded(bar_o, 0, p.status);
+    stage_v(1);
+    sync_tiles();                  // also: this chunk's raw pages are no longer read
+    if (ok && tid == 0) {
+      mma_o(1, ci == 0);
+      if (ci + 2 < nck) issue(ci + 2);
+    }
+    if (ok) issued = min(nck, ci + 3);
+    if (ok) ok = mbar_wait_bounded(bar_o, 1, p.status);
+    ok = !__syncthreads_or(!ok);
   }
-  sync_tiles();
-  if (ok) l_row = xl[rl] + xl[kTileRows + rl];
-  if (ok && tid == 0) mma_o(0);
-  // second half of V once the first half's MMAs have read the buffer
-  if (ok) ok = mbar_wait_bounded(bar_o, 0, p.status);
-  stage_v(1);
-  sync_tiles();
-  if (ok && tid == 0) mma_o(1);
-  if (ok) ok = mbar_wait_bounded(bar_o, 1, p.status);
-  ok = !__syncthreads_or(!ok);
 
-  if (ok) {
+  if (ok && nck > 0) {
     tc::fence_after_sync();
-    // o = O * v_post / l into padded shared-memory rows (Q, K^, P and V^T are
-    // no longer read)
+    // o = O * v_post / l into padded shared-memory rows (Q, K^, P, V^T and the
+    // raw buffers are no longer read); a row without keys writes zeros
     const float inv = l_row > 0.f ? p.v_post / l_row : 0.f;
 #pragma unroll 1
     for (int k0 = 0; k0 < D / 2; k0 += 32) {
@@ -579,22 +637,23 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
         sts128(sb + OFF_Q + rl * ROWB + (colh * (D / 2) + k0 + e) * 4,
-               make_uint4(__float_as_uint(__uint_as_float(orr[e]) * inv),
-                          __float_as_uint(__uint_as_float(orr[e + 1]) * inv),
-                          __float_as_uint(__uint_as_float(orr[e + 2]) * inv),
-                          __float_as_uint(__uint_as_float(orr[e + 3]) * inv)));
+               l_row > 0.f ? make_uint4(__float_as_uint(__uint_as_float(orr[e]) * inv),
+                                        __float_as_uint(__uint_as_float(orr[e + 1]) * inv),
+                                        __float_as_uint(__uint_as_float(orr[e + 2]) * inv),
+                                        __float_as_uint(__uint_as_float(orr[e + 3]) * inv))
+                           : make_uint4(0, 0, 0, 0));
     }
   }
-  if (colh == 0) xlse[rl] = ok && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
+  if (colh == 0) xlse[rl] = ok && nck > 0 && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
 
-  // The CTAs of a cluster hold consecutive chunks of the same rows: CTA rank
-  // c merges rows c * 128/CL .. of every CTA's shared memory (log-sum-exp) and
-  // writes one partial per row for the cluster's chunks, with coalesced
-  // stores.  The second cluster barrier keeps each CTA's rows in place until
-  // its peers have read them.
+  // The CTAs of a cluster hold consecutive chunk ranges of the same rows: CTA
+  // rank c merges rows c * 128/CL .. of every CTA's shared memory (log-sum-exp)
+  // and writes one partial per row for the cluster, with coalesced stores.  The
+  // second cluster barrier keeps each CTA's rows in place until its peers have
+  // read them.
   const int CL = p.cluster;
   const uint32_t crank = cluster_ctarank();
-  const int part = chunk / CL;
+  const int part = blockIdx.x / CL;
   const int rpc = kTileRows / CL;
   cluster_sync();
   for (int lr = static_cast<int>(crank) * rpc + warp; lr < (static_cast<int>(crank) + 1) * rpc; lr += kThreads / 32) {
@@ -642,15 +701,19 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   // of the prefix (flags only, off the critical path; one KV head checks).
   if (kvh == 0) {
     const int b_first = r0 / rows_per_seq, b_last = (min(rows, r0 + kTileRows) - 1) / rows_per_seq;
-    for (int i = tid; i < (b_last - b_first + 1) * npg; i += kThreads) {
-      const int b = b_first + i / npg, j = tok0 / kPage + i % npg;
-      if (p.page_table[static_cast<size_t>(b) * p.max_pages + j] != p.page_table[j])
+    const int pages = nck * NPG;
+    for (int i = tid; i < (b_last - b_first + 1) * pages; i += kThreads) {
+      const int bb = b_first + i / pages, j = c0 * NPG + i % pages;
+      if (j * kPage < p.prefix_len && p.page_table[static_cast<size_t>(bb) * p.max_pages + j] != p.page_table[j])
         flag_error(p.status, MEMRA_DEVERR_PREFIX);
     }
-    if (chunk == 0)
-      for (int b = b_first + tid; b <= b_last; b += kThreads)
-        if (p.seq_lens[b] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
+    if (blockIdx.x == 0)
+      for (int bb = b_first + tid; bb <= b_last; bb += kThreads)
+        if (p.seq_lens[bb] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
   }
+  // After a wait that gave up, the copies still in flight land (bounded) before the CTA leaves.
+  if (!ok)
+    for (int ci = consumed; ci < issued; ++ci) mbar_wait_bounded(bar_raw0 + 8 * (ci & 1), (ci >> 1) & 1, p.status);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
@@ -740,13 +803,14 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
 
 template <int D, int KF, int VF>
 cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
-  constexpr uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D));
+  const uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), p.cpc);
+  constexpr uint32_t smem_max = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), kCascadeMaxChunksPerCta);
   // any mix of prefix-pass CTAs that fits an SM by shared memory fits its tensor memory
-  constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128) + 1024u;   // smallest CTAs
-  constexpr uint32_t kMin256 = cascade_smem_bytes(256, 9 * 256, 9 * 256) + 1024u;
-  static_assert(4u * kMin128 > 233472u && 3u * cascade_tmem_cols(128) <= 512u, "three 128s at most");
-  static_assert(2u * kMin256 > 233472u && kMin256 + 2u * kMin128 > 233472u &&
-                    cascade_tmem_cols(256) + cascade_tmem_cols(128) <= 512u, "one 256 and one 128 at most");
+  constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128, 1) + 1024u;   // smallest CTAs
+  constexpr uint32_t kMin256 = cascade_smem_bytes(256, 9 * 256, 9 * 256, 1) + 1024u;
+  static_assert(3u * kMin128 > 233472u && 2u * cascade_tmem_cols(128) <= 512u, "two 128s at most");
+  static_assert(2u * kMin256 > 233472u && kMin256 + kMin128 > 233472u && cascade_tmem_cols(256) <= 512u,
+                "one 256 and nothing else");
   auto kernel = cascade_prefix_kernel<D, KF, VF>;
   // Cluster size, per device and instantiation: the largest of 8, 4, 2 whose
   // co-resident clusters still cover 90% of the CTA slots (on 152 SMs,
@@ -758,12 +822,14 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!widest[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    // the one-chunk plan decides, whatever the first call's chunks per CTA
+    const uint32_t smem1 = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), 1);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem1);
     if (e != cudaSuccess) return e;
     const int slots = sms * (per_sm > 0 ? per_sm : 1);
     int w = 1;
@@ -771,7 +837,7 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem;
+      cfg.dynamicSmemBytes = smem1;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
@@ -788,10 +854,11 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
     }
     widest[dev] = w;
   }
+  const int n_ctas = (p.n_chunks + p.cpc - 1) / p.cpc;      // CTAs per (KV head, row tile)
   int cl = widest[dev];
-  while (cl > 1 && cl > p.n_chunks) cl /= 2;
+  while (cl > 1 && cl > n_ctas) cl /= 2;
   p.cluster = cl;
-  p.n_parts = (p.n_chunks + cl - 1) / cl;
+  p.n_parts = (n_ctas + cl - 1) / cl;
   const int rows = p.batch * p.q_len * p.group;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.n_parts * cl), static_cast<unsigned>(p.n_kv_heads),

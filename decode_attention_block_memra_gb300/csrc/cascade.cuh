@@ -27,8 +27,9 @@ struct CascadeParams {
   float *o_pre;       // [batch * q_len * n_heads][n_parts][D], row id (b * q_len + i) * n_heads + h
   float *lse_pre;     // [batch * q_len * n_heads][n_parts]
   int batch, q_len, n_heads, group, n_kv_heads, num_pages, max_pages, prefix_len, n_chunks;
+  int cpc;            // chunks per CTA (1 .. kCascadeMaxChunksPerCta)
   int cluster;        // CTAs per cluster along the chunks (1, 2, 4 or 8), set by the launcher
-  int n_parts;        // prefix partials per row: ceil(n_chunks / cluster), set by the launcher
+  int n_parts;        // prefix partials per row: ceil(CTAs per row tile / cluster), set by the launcher
   float scale_log2;   // sm_scale * (post-scale of the staged K values) * log2(e)
   float v_post;       // post-scale of the staged V values
 };
@@ -45,21 +46,36 @@ struct CascadeCombineParams {
   int n_parts;            // prefix partials per row (CascadeParams::n_parts of the prefix pass)
 };
 
-// Shared memory of one prefix-pass CTA for head_dim D and the formats' segment bytes.
-__host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg) {
+// Chunks one prefix-pass CTA loops over at most.
+constexpr int kCascadeMaxChunksPerCta = 64;
+
+// Shared memory of one prefix-pass CTA for head_dim D, the formats' segment
+// bytes and cpc chunks per CTA: the Q tile, one half-chunk of K^ and of V^T
+// (hi and lo parts), the raw pages (two buffers when the CTA loops), the
+// softmax exchange, the page ids, the barriers.
+// At head_dim 256 the request is at least 155 KiB, so that no head_dim-128 CTA
+// (and its tensor memory) fits beside it.
+__host__ __device__ constexpr uint32_t cascade_smem_plan(int D, int kseg, int vseg, int cpc) {
   return 128u * D * 2 + 2u * cascade_chunk_tokens(D) * D * 2 +
-         static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 64u;
+         (cpc > 1 ? 2u : 1u) * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) +
+         5u * 128u * 4u + 4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 64u;
+}
+__host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg, int cpc) {
+  return D == 256 && cascade_smem_plan(D, kseg, vseg, cpc) < 155u * 1024u ? 155u * 1024u
+                                                                           : cascade_smem_plan(D, kseg, vseg, cpc);
 }
 
-// Tensor-memory columns of one prefix-pass CTA: the O accumulator's head_dim
-// columns, which also hold the chunk's scores S until the softmax has read
-// them (the first O MMA overwrites them).  The hardware places CTAs, and whole
-// clusters, by registers and shared memory, not by tensor memory, so any mix
-// of prefix-pass CTAs that fits an SM by shared memory must fit its 512
-// columns: at most three of head_dim 128 (>= 74 KB each, 384 columns) or one
-// of each head_dim (384 columns).  A CTA that found the columns taken would
-// wait in its allocation while its cluster peers wait for it.
-__host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) { return static_cast<uint32_t>(D); }
+// Tensor-memory columns of one prefix-pass CTA: O (head_dim columns) and the
+// chunk's scores S, rounded up to a power of two (256 at head_dim 128, 512 at
+// 256).  The hardware places CTAs, and whole clusters, by registers and shared
+// memory, not by tensor memory, so any mix of prefix-pass CTAs that fits an SM
+// by shared memory must fit its 512 columns: two of head_dim 128 (>= 76 KB
+// each, so never three) or one of head_dim 256 (>= 148 KB, with no room for a
+// 128 beside it).  A CTA that found the columns taken would wait in its
+// allocation while its cluster peers wait for it.
+__host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) {
+  return D + cascade_chunk_tokens(D) <= 256 ? 256u : 512u;
+}
 
 // Chooses the cluster size (the largest of 8, 4, 2, 1 not above n_chunks that
 // the device can co-schedule), fills p.cluster and p.n_parts, and launches.

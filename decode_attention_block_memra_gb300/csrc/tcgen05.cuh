@@ -93,5 +93,19 @@ __device__ __forceinline__ void wait_ld(uint32_t *r) {
                : "memory");
 }
 
+// Whole warp: the store counterpart of ld_32x32b_x16 (lane i of the warp
+// writes its 16 registers to tensor-memory lane (lane field of `taddr`) + i).
+__device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Whole warp: this thread's earlier tensor-memory stores have completed.
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 }  // namespace tc
 }  // namespace memra

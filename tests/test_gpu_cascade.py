@@ -204,3 +204,33 @@ def test_cascade_edges(case):
     res = run(w, fused=True)
     assert res.flags == 0
     assert_close(w, res.out, attention.reference(w))
+
+
+@pytest.mark.parametrize("D,n_kv_heads,prefix,q_len", [(128, 1, 40960, 2), (256, 2, 16384, 1)])
+def test_cascade_ctas_loop_over_chunks(D, n_kv_heads, prefix, q_len):
+    # more chunks than one wave of CTAs per KV head: each prefix CTA loops over several
+    w = small(D=D, n_heads=8 * n_kv_heads, n_kv_heads=n_kv_heads, q_len=q_len, prefix=prefix,
+              seq_lens=(prefix + 40, prefix + 700, prefix + 1500), seed=41)
+    res = run(w, fused=True)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+def test_cascade_rescales_the_accumulator():
+    # keys of one prefix chunk 8x larger: the row maxima jump by far more than the lazy margin.  With
+    # 640 chunks over 304 CTA slots a CTA takes 3 chunks, so chunk 301 (tokens 19,264 .. 19,327; prefix
+    # rows are stored in token order) is the second of its CTA, which rescales O in tensor memory
+    w = small(n_heads=8, n_kv_heads=1, prefix=40960, seq_lens=(41000, 41600), seed=42)
+    k = w.k_rows.astype(np.float32)
+    k[19264:19328] *= 8.0
+    w.k_rows = k.astype(np.float16)
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))
+
+
+def test_cascade_full_size_long_shared_prefix():
+    w = W.shared_prefix_long()
+    res = run(w, fused=True)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))

@@ -260,6 +260,14 @@ def shared_prefix() -> Workload:
                          seq_lens=[4860] * 16, shared_prefix=4096)
 
 
+def shared_prefix_long() -> Workload:
+    """16 sequences of 33,532 tokens sharing a 32,768-token prefix (a long shared document or system
+    prompt before each request's own 764 tokens), 32/4 heads, D 128, seed 6."""
+    return make_workload("shared_prefix_long_b16_ctx33532_prefix32768_h32kv4_d128", batch=16, q_len=1,
+                         n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0", v_fmt="q5_1", seed=6,
+                         seq_lens=[33532] * 16, shared_prefix=32768)
+
+
 def long_context() -> Workload:
     """batch 1, 262,144-token context, 32/4 heads, D 128, pages in a random permutation, k x0.5, seed 2."""
     return make_workload("long_context_b1_ctx262144_h32kv4_d128", batch=1, q_len=1, n_heads=32, n_kv_heads=4,
@@ -287,6 +295,7 @@ def format_sweep(variant: str = "c") -> Workload:
 WORKLOADS = {
     "tiny": tiny,
     "shared_prefix": shared_prefix,
+    "shared_prefix_long": shared_prefix_long,
     "long_context": long_context,
     "mtp_verify": mtp_verify,
     "sweep_a": lambda: format_sweep("a"),
