@@ -198,14 +198,18 @@ int check_decode(const DecodeArgs &a) {
   return MEMRA_OK;
 }
 
-// Chunks per prefix-pass CTA of a cascade call: enough CTAs per KV head for
-// one wave of one row tile, never more than kCascadeMaxChunksPerCta chunks
-// each.  Depends on the prefix, head_dim, KV heads and the device only.
-int cascade_cpc(int32_t prefix, int32_t head_dim, int32_t n_kv_heads) {
+// Chunks per prefix-pass CTA of a cascade call: few enough CTAs per KV head
+// that one row tile's fit one wave of the pass (as the device co-schedules its
+// clusters), never more than kCascadeMaxChunksPerCta chunks each.  Depends on
+// the prefix, head_dim, formats, KV heads and the device only.
+int cascade_cpc(int32_t prefix, int32_t head_dim, int kf, int vf, int32_t n_kv_heads, int *cpc) {
+  int cl = 1, wave = 1;
+  if (cascade_wave(head_dim, kf, vf, &cl, &wave) != cudaSuccess) return MEMRA_ERR_CUDA;
   const int64_t n_chunks = ceil_div(prefix, cascade_chunk_tokens(head_dim));
-  const int64_t target = std::max<int64_t>(1, device_sms() * cascade_ctas_per_sm(head_dim) / n_kv_heads);
-  return static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(n_chunks, target), 1),
+  const int64_t target = std::max<int64_t>(1, wave / n_kv_heads);
+  *cpc = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(n_chunks, target), 1),
                                             kCascadeMaxChunksPerCta));
+  return MEMRA_OK;
 }
 
 // k_new / v_new: the fused append's rows, or null for attention alone.
@@ -214,13 +218,17 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   Plan pl;
   const int group = a.n_heads / a.n_kv_heads;
   // a cascade call's own-key pass shares each SM with the prefix pass's CTAs
-  const int pre_per_sm = cascade_ctas_per_sm(a.head_dim);
-  const size_t cap = a.prefix > 0 ? kSmPerSm - kSmReservedPerCta * (1 + pre_per_sm) -
-                                        pre_per_sm * static_cast<size_t>(cascade_smem_bytes(
-                                                         a.head_dim, k_seg_bytes(c.k_fmt, a.head_dim),
-                                                         v_seg_bytes(c.v_fmt, a.head_dim),
-                                                         cascade_cpc(a.prefix, a.head_dim, a.n_kv_heads)))
-                                  : 0;
+  size_t cap = 0;
+  if (a.prefix > 0) {
+    int cpc = 1;
+    int rc0 = cascade_cpc(a.prefix, a.head_dim, c.k_fmt, c.v_fmt, a.n_kv_heads, &cpc);
+    if (rc0) return rc0;
+    const int pre_per_sm = cascade_ctas_per_sm(a.head_dim);
+    const size_t pre = pre_per_sm * static_cast<size_t>(cascade_smem_bytes(
+                                        a.head_dim, k_seg_bytes(c.k_fmt, a.head_dim), v_seg_bytes(c.v_fmt, a.head_dim), cpc));
+    const size_t used = kSmReservedPerCta * (1 + pre_per_sm) + pre;
+    cap = used < kSmPerSm ? kSmPerSm - used : 1;
+  }
   int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl, cap);
   if (rc) return rc;
   // keys this pass covers: all of them, or (cascade) those from the prefix end on
@@ -418,7 +426,8 @@ int cascade_passes(const DecodeArgs &a, const void *k_new, const void *v_new, vo
   cp.max_pages = a.max_pages_per_seq;
   cp.prefix_len = a.prefix;
   cp.n_chunks = n_chunks;
-  cp.cpc = cascade_cpc(a.prefix, a.head_dim, a.n_kv_heads);
+  st = cascade_cpc(a.prefix, a.head_dim, c.k_fmt, c.v_fmt, a.n_kv_heads, &cp.cpc);
+  if (st) return st;
   // staged values: q8_0 / q5_1 / q4_0 at half size, fp8 / NVFP4 without their tensor scale
   const float k_post = c.k_fmt == MEMRA_KV_Q8_0 ? 2.f : c.k_scale;
   cp.scale_log2 = a.sm_scale * k_post * 1.4426950408889634f;

@@ -802,8 +802,7 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
 }
 
 template <int D, int KF, int VF>
-cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
-  const uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), p.cpc);
+cudaError_t wave_one(int *cluster, int *wave_ctas) {
   constexpr uint32_t smem_max = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), kCascadeMaxChunksPerCta);
   // any mix of prefix-pass CTAs that fits an SM by shared memory fits its tensor memory
   constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128, 1) + 1024u;   // smallest CTAs
@@ -812,11 +811,16 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   static_assert(2u * kMin256 > 233472u && kMin256 + kMin128 > 233472u && cascade_tmem_cols(256) <= 512u,
                 "one 256 and nothing else");
   auto kernel = cascade_prefix_kernel<D, KF, VF>;
-  // Cluster size, per device and instantiation: the largest of 8, 4, 2 whose
-  // co-resident clusters still cover 90% of the CTA slots (on 152 SMs,
-  // clusters of 8 CTAs of 197 KB fit only 15 at a time), else 1.
-  // It depends on the device and the formats only, never on the batch.
-  static int widest[64] = {};
+  // Per device and instantiation, for the largest footprint (a CTA that loops):
+  // the cluster size, the largest of 8, 4, 2 whose co-resident clusters place
+  // at least 90% of the CTAs that single CTAs would (on 152 SMs, clusters of 8
+  // of these CTAs fit only 15 at a time), else 1; and the CTAs one wave holds.
+  // The wave is the SMs times the CTAs per SM the kernel is built for (two at
+  // head_dim 128: registers, shared memory and tensor memory allow it, and
+  // traces show them co-resident), scaled by that cluster fraction; the
+  // occupancy query itself reports one CTA per SM for this kernel.  Both depend
+  // on the device and the formats only, never on the batch.
+  static int widest[64] = {}, wave[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -824,20 +828,18 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   if (!widest[dev]) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
     if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
+    // all of the SM's unified L1 / shared memory as shared memory, so that two
+    // CTAs of ~100 KB share an SM
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // the one-chunk plan decides, whatever the first call's chunks per CTA
-    const uint32_t smem1 = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), 1);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem1);
-    if (e != cudaSuccess) return e;
-    const int slots = sms * (per_sm > 0 ? per_sm : 1);
-    int w = 1;
-    for (int cl = 8; cl > 1; cl /= 2) {
+    auto active = [&](int cl) {      // co-resident clusters of cl CTAs, as the occupancy query counts them
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem1;
+      cfg.dynamicSmemBytes = smem_max;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
@@ -846,16 +848,39 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && 10 * n * cl >= 9 * slots) {
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();          // a refused query is not an error of this call
+        n = 0;
+      }
+      return n;
+    };
+    const int single = active(1);
+    const int slots = sms * cascade_ctas_per_sm(D);
+    int w = 1, ctas = slots;
+    for (int cl = 8; cl > 1 && single > 0; cl /= 2) {
+      const int n = active(cl);
+      if (10 * n * cl >= 9 * single) {
         w = cl;
+        ctas = static_cast<int>(static_cast<int64_t>(slots) * n * cl / single);
         break;
       }
-      cudaGetLastError();    // a refused query is not an error of this call
     }
+    wave[dev] = ctas > 0 ? ctas : 1;
     widest[dev] = w;
   }
+  *cluster = widest[dev];
+  *wave_ctas = wave[dev];
+  return cudaSuccess;
+}
+
+template <int D, int KF, int VF>
+cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
+  int cl = 1, wave = 1;
+  cudaError_t e = wave_one<D, KF, VF>(&cl, &wave);     // also sets the shared-memory limit once
+  if (e != cudaSuccess) return e;
+  const uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), p.cpc);
+  auto kernel = cascade_prefix_kernel<D, KF, VF>;
   const int n_ctas = (p.n_chunks + p.cpc - 1) / p.cpc;      // CTAs per (KV head, row tile)
-  int cl = widest[dev];
   while (cl > 1 && cl > n_ctas) cl /= 2;
   p.cluster = cl;
   p.n_parts = (n_ctas + cl - 1) / cl;
@@ -877,6 +902,26 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   cfg.numAttrs = 2;
   const CascadeParams args = p;
   return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
+template <int D>
+cudaError_t wave_formats(int kf, int vf, int *cluster, int *wave_ctas) {
+  auto by_v = [&](auto kc) -> cudaError_t {
+    constexpr int K = decltype(kc)::value;
+    switch (vf) {
+      case MEMRA_KV_Q5_1: return wave_one<D, K, MEMRA_KV_Q5_1>(cluster, wave_ctas);
+      case MEMRA_KV_Q4_0: return wave_one<D, K, MEMRA_KV_Q4_0>(cluster, wave_ctas);
+      case MEMRA_KV_FP8_E4M3: return wave_one<D, K, MEMRA_KV_FP8_E4M3>(cluster, wave_ctas);
+      case MEMRA_KV_NVFP4: return wave_one<D, K, MEMRA_KV_NVFP4>(cluster, wave_ctas);
+      default: return cudaErrorInvalidValue;
+    }
+  };
+  switch (kf) {
+    case MEMRA_KV_Q8_0: return by_v(std::integral_constant<int, MEMRA_KV_Q8_0>{});
+    case MEMRA_KV_FP8_E4M3: return by_v(std::integral_constant<int, MEMRA_KV_FP8_E4M3>{});
+    case MEMRA_KV_NVFP4: return by_v(std::integral_constant<int, MEMRA_KV_NVFP4>{});
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int D>
@@ -904,6 +949,10 @@ cudaError_t prefix_formats(int kf, int vf, CascadeParams &p, cudaStream_t st) {
 cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st) {
   if (p.n_chunks == 0 || p.batch == 0) return cudaSuccess;
   return D == 128 ? prefix_formats<128>(kf, vf, p, st) : prefix_formats<256>(kf, vf, p, st);
+}
+
+cudaError_t cascade_wave(int D, int kf, int vf, int *cluster, int *wave_ctas) {
+  return D == 128 ? wave_formats<128>(kf, vf, cluster, wave_ctas) : wave_formats<256>(kf, vf, cluster, wave_ctas);
 }
 
 cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st) {

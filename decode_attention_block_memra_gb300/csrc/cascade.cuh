@@ -77,8 +77,12 @@ __host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) {
   return D + cascade_chunk_tokens(D) <= 256 ? 256u : 512u;
 }
 
-// Chooses the cluster size (the largest of 8, 4, 2, 1 not above n_chunks that
-// the device can co-schedule), fills p.cluster and p.n_parts, and launches.
+// The prefix pass's cluster size on this device for these formats and the
+// CTAs one wave of it holds (both independent of the batch).
+cudaError_t cascade_wave(int D, int kf, int vf, int *cluster, int *wave_ctas);
+
+// Narrows the cluster size to the CTAs per row tile, fills p.cluster and
+// p.n_parts, and launches.
 cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st);
 cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st);
 
