@@ -162,14 +162,15 @@ __device__ __forceinline__ void convert_k8(const KRaw &r, int t, uint32_t (&hi)[
 }
 
 // Raw words of one V staging task of the q5_1 / q4_0 / fp8 layouts: page half
-// ph, block b, dim group vg (dims 32 b + 4 vg .. + 3), tokens 8 ph + 2 c + f.
+// ph, block b, dim group vg and pair h (dims 32 b + 4 vg + 2 h, + 1), tokens
+// 8 ph + 2 c + f.
 struct VRaw {
-  uint2 lw[4];                 // per c: the h = 0 and h = 1 code words
+  uint32_t lw[4];              // per c: the code word of pair h
   uint32_t hw[4], dw[4], mw[4];
 };
 
 template <int D, int VF>
-__device__ __forceinline__ VRaw load_v_task(uint32_t seg, int ph, int b, int vg) {
+__device__ __forceinline__ VRaw load_v_task(uint32_t seg, int ph, int b, int vg, int h) {
   constexpr int NB = D / 32;
   VRaw r;
 #pragma unroll
@@ -177,11 +178,10 @@ __device__ __forceinline__ VRaw load_v_task(uint32_t seg, int ph, int b, int vg)
     const uint32_t lane = 4 * vg + c;
     r.hw[c] = r.dw[c] = r.mw[c] = 0u;
     if constexpr (VF == MEMRA_KV_FP8_E4M3) {
-      r.lw[c].x = lds32(seg + (b * 32 + lane) * 16 + 4 * ph);
-      r.lw[c].y = lds32(seg + (b * 32 + lane) * 16 + 8 + 4 * ph);
+      r.lw[c] = lds32(seg + (b * 32 + lane) * 16 + 8 * h + 4 * ph);
     } else {
       const uint32_t doff = ((c * NB + b) * 4 + 2 * ph) * 2;
-      r.lw[c] = lds64(seg + ((b >> 1) * 32 + lane) * 16 + (b & 1) * 8);
+      r.lw[c] = lds32(seg + ((b >> 1) * 32 + lane) * 16 + (b & 1) * 8 + 4 * h);
       if constexpr (VF == MEMRA_KV_Q5_1) {
         r.hw[c] = lds32(seg + 8 * D + (lane * (NB / 2) + (b >> 1)) * 4);
         r.dw[c] = lds32(seg + 10 * D + doff);
@@ -194,19 +194,16 @@ __device__ __forceinline__ VRaw load_v_task(uint32_t seg, int ph, int b, int vg)
   return r;
 }
 
-// The task's values: for dim e = 2 h + s of the group, tokens 2c, 2c + 1 as one
-// fp16 pair hi[e][c] (and lo[e][c] for q5_1 / q4_0).
+// The task's values: for dim s of the pair, tokens 2c, 2c + 1 as one fp16
+// pair hi[s][c] (and lo[s][c] for q5_1 / q4_0).
 template <int VF>
-__device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, uint32_t (&hi)[4][4],
-                                               uint32_t (&lo)[4][4]) {
+__device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, int h, uint32_t (&hi)[2][4],
+                                               uint32_t (&lo)[2][4]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     if constexpr (VF == MEMRA_KV_FP8_E4M3) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // bytes 2 s + f of the word: (s = 0: f = 0, 1), (s = 1: f = 0, 1)
-        e4m3x4_to_half2x2(h ? r.lw[c].y : r.lw[c].x, hi[2 * h][c], hi[2 * h + 1][c]);
-      }
+      // bytes 2 s + f of the word: (s = 0: f = 0, 1), (s = 1: f = 0, 1)
+      e4m3x4_to_half2x2(r.lw[c], hi[0][c], hi[1][c]);
     } else {
       float dh[2], mh[2];
 #pragma unroll
@@ -215,28 +212,24 @@ __device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, uin
         mh[f] = 0.5f * __half2float(__ushort_as_half(static_cast<unsigned short>(r.mw[c] >> (16 * f))));
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int s = 0; s < 2; ++s) {
+        float x[2];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          float x[2];
-#pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            const int k = 2 * f + ph;
-            const uint32_t word = h ? r.lw[c].y : r.lw[c].x;
-            uint32_t q = (word >> (8 * k + 4 * s)) & 15u;
-            // the code as an exact float: 2^23 + q, less 2^23 (q5_1) or 2^23 + 8 (q4_0)
-            if constexpr (VF == MEMRA_KV_Q5_1) {
-              q |= ((r.hw[c] >> (8 * k + 4 * s + 2 * (b & 1) + h)) & 1u) << 4;
-              x[f] = fmaf(dh[f], __uint_as_float(0x4B000000u | q) - 8388608.f, mh[f]);
-            } else {
-              x[f] = dh[f] * (__uint_as_float(0x4B000000u | q) - 8388616.f);
-            }
+        for (int f = 0; f < 2; ++f) {
+          const int k = 2 * f + ph;
+          uint32_t q = (r.lw[c] >> (8 * k + 4 * s)) & 15u;
+          // the code as an exact float: 2^23 + q, less 2^23 (q5_1) or 2^23 + 8 (q4_0)
+          if constexpr (VF == MEMRA_KV_Q5_1) {
+            q |= ((r.hw[c] >> (8 * k + 4 * s + 2 * (b & 1) + h)) & 1u) << 4;
+            x[f] = fmaf(dh[f], __uint_as_float(0x4B000000u | q) - 8388608.f, mh[f]);
+          } else {
+            x[f] = dh[f] * (__uint_as_float(0x4B000000u | q) - 8388616.f);
           }
-          const __half2 h2 = __floats2half2_rn(x[0], x[1]);
-          const float2 back = __half22float2(h2);
-          hi[2 * h + s][c] = h2_bits(h2);
-          lo[2 * h + s][c] = h2_bits(__floats2half2_rn(x[0] - back.x, x[1] - back.y));
         }
+        const __half2 h2 = __floats2half2_rn(x[0], x[1]);
+        const float2 back = __half22float2(h2);
+        hi[s][c] = h2_bits(h2);
+        lo[s][c] = h2_bits(__floats2half2_rn(x[0] - back.x, x[1] - back.y));
       }
     }
   }
@@ -281,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
                 "alignment");
   constexpr int QIT = kTileRows * (D / 8) / kThreads;        // Q items per thread
   constexpr int KIT = H * (D / 8) / kThreads;                // K items per thread and half
-  constexpr int VTASKS = VF == MEMRA_KV_NVFP4 ? HPG * 2 * (D / 16) * 8 : HPG * 2 * NB * 8;
+  constexpr int VTASKS = VF == MEMRA_KV_NVFP4 ? HPG * 2 * (D / 16) * 8 : HPG * 2 * NB * 8 * 2;
   constexpr int VIT = (VTASKS + kThreads - 1) / kThreads;    // V tasks per thread and half
   static_assert(QIT * kThreads == kTileRows * (D / 8) && KIT * kThreads == H * (D / 8), "whole items");
   static_assert(VIT * kThreads == VTASKS || (VIT == 1 && VTASKS % 32 == 0), "whole warps of tasks");
@@ -454,29 +447,30 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
         vt_store(16 * b16 + rr + 8, 2 * psl + ph, make_uint4(h1[0], h1[1], h1[2], h1[3]), z);
       }
     } else {
-      // task (page, half page, block b, vg): dims 32 b + 4 vg + (2 h + s), tokens 8 half + 2 c + f
+      // task (page, half page, block b, vg, pair h): dims 32 b + 4 vg + 2 h + s, tokens 8 half + 2 c + f
       VRaw vr[VIT];
 #pragma unroll
       for (int it = 0; it < VIT; ++it) {
         const int task = tid + it * kThreads;
         if (task >= VTASKS) break;
-        const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1,
-                  ps = hf * HPG + task / (16 * NB);
-        vr[it] = load_v_task<D, VF>(rawv + ps * VSEG, ph, b, vg);
+        const int h = task & 1, vg = (task >> 1) & 7, b = (task >> 4) % NB, ph = (task / (16 * NB)) & 1,
+                  ps = hf * HPG + task / (32 * NB);
+        vr[it] = load_v_task<D, VF>(rawv + ps * VSEG, ph, b, vg, h);
       }
 #pragma unroll
       for (int it = 0; it < VIT; ++it) {
         const int task = tid + it * kThreads;
         if (task >= VTASKS) break;
-        const int vg = task & 7, b = (task >> 3) % NB, ph = (task / (8 * NB)) & 1, psl = task / (16 * NB);
-        uint32_t hi[4][4], lo[4][4];
-        convert_v_task<VF>(vr[it], ph, b, hi, lo);
+        const int h = task & 1, vg = (task >> 1) & 7, b = (task >> 4) % NB, ph = (task / (16 * NB)) & 1,
+                  psl = task / (32 * NB);
+        uint32_t hi[2][4], lo[2][4];
+        convert_v_task<VF>(vr[it], ph, b, h, hi, lo);
         const bool have = ok && ((pmask >> (hf * HPG + psl)) & 1u);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint4 h = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
-          const uint4 l = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
-          vt_store(32 * b + 4 * vg + e, 2 * psl + ph, h, l);
+        for (int e = 0; e < 2; ++e) {
+          const uint4 hv = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
+          const uint4 lv = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
+          vt_store(32 * b + 4 * vg + 2 * h + e, 2 * psl + ph, hv, lv);
         }
       }
     }
