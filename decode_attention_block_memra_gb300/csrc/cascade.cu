@@ -713,6 +713,517 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
 }
 
+// Warps of the warp-specialized pass: 4 softmax, kStageWarps staging, 1 MMA.
+constexpr int kStageWarps = 8;
+constexpr int kStageThreads = 32 * kStageWarps;
+constexpr int kMmaWarp = 4 + kStageWarps;
+constexpr int kWsThreads = 32 * (kMmaWarp + 1);
+
+// Staging warps of the warp-specialized pass (named barrier 1): a barrier that
+// also ANDs `ok` over them, so that they all take the same branch.
+__device__ __forceinline__ bool staging_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u), "n"(kStageThreads)
+      : "memory");
+  return r != 0;
+}
+
+// The head_dim 128 prefix pass, warp-specialized: the three kinds of work of a
+// chunk (dequantizing K and V into tensor-core tiles, the MMAs, the online
+// softmax) run in separate warps and overlap across chunks through
+// double-buffered tiles handed over by mbarriers.
+//   * warps 0-3 (softmax): thread = query row; per chunk it reads the row's
+//     scores from tensor memory, keeps the row's reference maximum (moved only
+//     when a chunk passes it by more than kLazy, in log2 units), rescales O in
+//     tensor memory when it moves, writes P (fp16) for the output MMA, and at
+//     the end normalizes O;
+//   * warps 4 .. 4 + kStageWarps - 1 (staging): per chunk, waits for its
+//     pages, dequantizes K and V into the buffers the MMAs of two chunks ago
+//     have released, and issues the copies of the chunk after next;
+//   * warp kMmaWarp, one thread (MMA): S(i) = Q K(i)^T into one of two
+//     tensor-memory score buffers as soon as K(i) is staged, then
+//     O += P(i-1) V(i-1).
+// Tensor memory: O in columns 0..127, the two score buffers in 128..191 and
+// 192..255.  One CTA per SM (228 KB of shared memory).
+template <int KF, int VF>
+__global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const CascadeParams p) {
+  constexpr int D = 128;
+  constexpr int NC = cascade_chunk_tokens(D);       // 64 prefix tokens per chunk
+  constexpr int NPG = NC / kPage;
+  constexpr int NB = D / 32;
+  constexpr int KSEG = k_seg_bytes(KF, D);
+  constexpr int VSEG = v_seg_bytes(VF, D);
+  constexpr bool kKLo = KF == MEMRA_KV_Q8_0;
+  constexpr bool kVLo = VF == MEMRA_KV_Q5_1 || VF == MEMRA_KV_Q4_0;
+  constexpr float kLazy = 8.f;                      // log2 units: P stays <= 256 between rescales
+  // Shared memory: Q tile | K^ buffers [2] (hi, lo) | V^T buffers [2] (hi, lo)
+  // | P buffers [2] | raw page buffers [2] | row lse | page ids | barriers.
+  // The output rows reuse Q and the K^ buffers once the last MMA is done.
+  constexpr uint32_t QB = kTileRows * D * 2, KB = NC * D * 2, VB = D * NC * 2, PB = kTileRows * NC * 2;
+  constexpr uint32_t RAWB = NPG * (KSEG + VSEG);
+  constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 4 * KB, OFF_P = OFF_V + 4 * VB, OFF_RAW = OFF_P + 2 * PB,
+                     OFF_X = OFF_RAW + 2 * RAWB, OFF_PID = OFF_X + kTileRows * 4;
+  constexpr uint32_t ROWB = D * 4 + 16;
+  constexpr uint32_t TCOLS = cascade_tmem_cols(D);
+  static_assert(OFF_PID + 4 * NPG * kCascadeMaxChunksPerCta + 192 ==
+                    cascade_smem_bytes(D, KSEG, VSEG, kCascadeMaxChunksPerCta), "shared-memory plan");
+  static_assert(cascade_smem_bytes(D, KSEG, VSEG, kCascadeMaxChunksPerCta) <= kSmemLimit, "shared memory");
+  static_assert(kTileRows * ROWB <= OFF_V, "output rows over Q and the K^ buffers");
+  static_assert(D + 2 * NC <= static_cast<int>(TCOLS), "O and two score buffers fit the tensor memory");
+  static_assert(KSEG % 16 == 0 && VSEG % 16 == 0 && RAWB % 16 == 0 && OFF_RAW % 16 == 0, "alignment");
+  constexpr int QIT = kTileRows * (D / 8) / 256;               // Q items per thread of warps 0-7
+  constexpr int KIT = NC * (D / 8) / kStageThreads;            // K items per staging thread and chunk
+  constexpr int VTASKS = VF == MEMRA_KV_NVFP4 ? NPG * 2 * (D / 16) * 8 : NPG * 2 * NB * 8 * 2;
+  constexpr int VIT = VTASKS / kStageThreads;                  // V tasks per staging thread and chunk
+  static_assert(QIT * 256 == kTileRows * (D / 8) && KIT * kStageThreads == NC * (D / 8) &&
+                    VIT * kStageThreads == VTASKS, "whole items");
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_addr(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t OFF_BAR = OFF_PID + 4 * NPG * p.cpc;
+  // barriers, two of each: raw pages landed, K^ staged / read, V^T staged / read,
+  // scores written / read, P written / read
+  const uint32_t bars = sb + OFF_BAR;
+  auto bar = [&](int kind, int b) { return bars + 16 * kind + 8 * b; };
+  enum { kRaw = 0, kKFull, kKEmpty, kVFull, kVEmpty, kSFull, kSEmpty, kPFull, kPEmpty };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 16 * 9);
+  int *pid_s = reinterpret_cast<int *>(smem + OFF_PID);
+  float *xlse = reinterpret_cast<float *>(smem + OFF_X);
+
+  const int kvh = blockIdx.y;
+  const int rows = p.batch * p.q_len * p.group;
+  const int r0 = blockIdx.z * kTileRows;
+  const int c0 = blockIdx.x * p.cpc;
+  const int nck = max(0, min(p.cpc, p.n_chunks - c0));
+  const int rows_per_seq = p.q_len * p.group;
+
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(smem_addr(tmem_slot), TCOLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32 * kMmaWarp) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kRaw, b), 1);
+      mbar_init(bar(kKFull, b), kStageThreads);
+      mbar_init(bar(kKEmpty, b), 1);
+      mbar_init(bar(kVFull, b), kStageThreads);
+      mbar_init(bar(kVEmpty, b), 1);
+      mbar_init(bar(kSFull, b), 1);
+      mbar_init(bar(kSEmpty, b), 128);
+      mbar_init(bar(kPFull, b), 128);
+      mbar_init(bar(kPEmpty, b), 1);
+    }
+    fence_barrier_init();
+  }
+  grid_dependency_wait();          // q, the pools and the tables are written
+  allow_dependent_launch();
+
+  for (int i = tid; i < nck * NPG; i += kWsThreads) {
+    const int tok = c0 * NC + i * kPage;
+    int pid = -1;
+    if (tok < p.prefix_len) {
+      pid = p.page_table[tok / kPage];
+      if (pid < 0 || pid >= p.num_pages) {
+        flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+        pid = -1;
+      }
+    }
+    pid_s[i] = pid;
+  }
+  uint4 qv[QIT];
+  if (tid < 256) {
+#pragma unroll
+    for (int it = 0; it < QIT; ++it) {
+      const int i = tid + it * 256;
+      const int rest = i >> 3, u = rest % (D / 8);
+      const int r = r0 + (rest / (D / 8)) * 8 + (i & 7);
+      qv[it] = make_uint4(0, 0, 0, 0);
+      if (r < rows) {
+        const int b = r / rows_per_seq, rem = r % rows_per_seq;
+        const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                             rem % p.group;
+        qv[it] = *reinterpret_cast<const uint4 *>(p.q + rowid * D + 8 * u);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const size_t kstride = static_cast<size_t>(p.n_kv_heads) * KSEG, vstride = static_cast<size_t>(p.n_kv_heads) * VSEG;
+  auto issue = [&](int ci) {       // chunk ci's pages into raw buffer ci % 2
+    const uint32_t buf = sb + OFF_RAW + (ci & 1) * RAWB, br = bar(kRaw, ci & 1);
+    uint32_t bytes = 0;
+    for (int i = 0; i < NPG; ++i) bytes += pid_s[ci * NPG + i] >= 0 ? KSEG + VSEG : 0;
+    if (!bytes) {
+      mbar_arrive(br);
+      return;
+    }
+    mbar_arrive_expect_tx(br, bytes);
+    for (int i = 0; i < NPG; ++i) {
+      const int pg = pid_s[ci * NPG + i];
+      if (pg < 0) continue;
+      bulk_copy_g2s_nohint(buf + i * KSEG, p.k_pool + pg * kstride + static_cast<size_t>(kvh) * KSEG, KSEG, br);
+      bulk_copy_g2s_nohint(buf + NPG * KSEG + i * VSEG, p.v_pool + pg * vstride + static_cast<size_t>(kvh) * VSEG,
+                           VSEG, br);
+    }
+  };
+  auto chunk_mask = [&](int ci) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < NPG; ++i) m |= (pid_s[ci * NPG + i] >= 0 ? 1u : 0u) << i;
+    return m;
+  };
+  if (tid == 128) {
+    if (nck > 0) issue(0);
+    if (nck > 1) issue(1);
+  }
+  if (tid < 256) {
+#pragma unroll
+    for (int it = 0; it < QIT; ++it) sts128(sb + OFF_Q + 16 * (tid + it * 256), qv[it]);
+    fence_proxy_async();           // the Q tile is read by the tensor cores
+  }
+  __syncthreads();
+
+  bool ok = true;
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ staging --
+    const int st = tid - 128;
+    int issued = min(nck, 2), consumed = 0;
+    for (int ci = 0; ci < nck && ok; ++ci) {
+      const int b = ci & 1, u = ci >> 1;
+      const uint32_t rawk = sb + OFF_RAW + b * RAWB, rawv = rawk + NPG * KSEG;
+      const uint32_t kbuf = sb + OFF_K + b * 2 * KB, vbuf = sb + OFF_V + b * 2 * VB;
+      const uint32_t pmask = chunk_mask(ci);
+      ok = mbar_wait_bounded(bar(kRaw, b), u & 1, p.status);
+      if (ok && ci >= 2) ok = mbar_wait_bounded(bar(kKEmpty, b), (u - 1) & 1, p.status);
+      ok = staging_all(ok);        // uniform over the staging warps: every one takes the same branch
+      if (!ok) break;
+      consumed = ci + 1;
+      {   // K^: item i = (token group, 8-dim group, token in group) at byte 16 i
+        KRaw kr[KIT];
+#pragma unroll
+        for (int it = 0; it < KIT; ++it) {
+          const int i = st + it * kStageThreads;
+          const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+          kr[it] = load_k8<D, KF>(rawk + (n / kPage) * KSEG, n % kPage, (i >> 3) % (D / 8));
+        }
+#pragma unroll
+        for (int it = 0; it < KIT; ++it) {
+          const int i = st + it * kStageThreads;
+          const int n = ((i >> 3) / (D / 8)) * 8 + (i & 7);
+          uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+          if ((pmask >> (n / kPage)) & 1u) convert_k8<KF>(kr[it], n % kPage, hi, lo);
+          sts128(kbuf + 16 * i, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+          if constexpr (kKLo) sts128(kbuf + KB + 16 * i, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(bar(kKFull, b));
+      if (ci >= 2) ok = mbar_wait_bounded(bar(kVEmpty, b), (u - 1) & 1, p.status);
+      ok = staging_all(ok);
+      if (!ok) break;
+      auto vt_store = [&](int dd, int g, uint4 h, uint4 l) {
+        const uint32_t off = ((dd >> 3) * (NC / 8) + g) * 128 + (dd & 7) * 16;
+        sts128(vbuf + off, h);
+        if constexpr (kVLo) sts128(vbuf + VB + off, l);
+      };
+      if constexpr (VF == MEMRA_KV_NVFP4) {
+        // task (page, half page, 16-dim block b16, rr): dims 16 b16 + rr and + 8
+        uint32_t cw[VIT][4], sw[VIT][4];
+#pragma unroll
+        for (int it = 0; it < VIT; ++it) {
+          const int task = st + it * kStageThreads;
+          const int rr = task & 7, b16 = (task >> 3) % (D / 16), ps = task / (16 * (D / 16));
+          const uint32_t seg = rawv + ps * VSEG;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            cw[it][c] = lds32(seg + ((b16 >> 2) * 32 + 4 * rr + c) * 16 + (b16 & 3) * 4);
+            sw[it][c] = lds32(seg + 8 * D + (c * (D / 16) + b16) * 4);
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < VIT; ++it) {
+          const int task = st + it * kStageThreads;
+          const int rr = task & 7, b16 = (task >> 3) % (D / 16), ph = (task / (8 * (D / 16))) & 1,
+                    ps = task / (16 * (D / 16));
+          uint32_t h0[4] = {0, 0, 0, 0}, h1[4] = {0, 0, 0, 0};
+          if ((pmask >> ps) & 1u) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              __half2 v[2];
+#pragma unroll
+              for (int f = 0; f < 2; ++f) {
+                const int sh = 8 * (f + 2 * ph);
+                v[f] = __hmul2(bits_h2(e2m1x2_to_half2((cw[it][c] >> sh) & 0xFFu)), e4m3_scale_h2(sw[it][c] >> sh));
+              }
+              h0[c] = h2_bits(__lows2half2(v[0], v[1]));
+              h1[c] = h2_bits(__highs2half2(v[0], v[1]));
+            }
+          }
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          vt_store(16 * b16 + rr, 2 * ps + ph, make_uint4(h0[0], h0[1], h0[2], h0[3]), z);
+          vt_store(16 * b16 + rr + 8, 2 * ps + ph, make_uint4(h1[0], h1[1], h1[2], h1[3]), z);
+        }
+      } else {
+        // task (page, half page, block b, vg, pair h): dims 32 b + 4 vg + 2 h + s, tokens 8 half + 2 c + f
+        VRaw vr[VIT];
+#pragma unroll
+        for (int it = 0; it < VIT; ++it) {
+          const int task = st + it * kStageThreads;
+          const int h = task & 1, vg = (task >> 1) & 7, bb = (task >> 4) % NB, ph = (task / (16 * NB)) & 1,
+                    ps = task / (32 * NB);
+          vr[it] = load_v_task<D, VF>(rawv + ps * VSEG, ph, bb, vg, h);
+        }
+#pragma unroll
+        for (int it = 0; it < VIT; ++it) {
+          const int task = st + it * kStageThreads;
+          const int h = task & 1, vg = (task >> 1) & 7, bb = (task >> 4) % NB, ph = (task / (16 * NB)) & 1,
+                    ps = task / (32 * NB);
+          uint32_t hi[2][4], lo[2][4];
+          convert_v_task<VF>(vr[it], ph, bb, h, hi, lo);
+          const bool have = (pmask >> ps) & 1u;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint4 hv = have ? make_uint4(hi[e][0], hi[e][1], hi[e][2], hi[e][3]) : make_uint4(0, 0, 0, 0);
+            const uint4 lv = have && kVLo ? make_uint4(lo[e][0], lo[e][1], lo[e][2], lo[e][3]) : make_uint4(0, 0, 0, 0);
+            vt_store(32 * bb + 4 * vg + 2 * h + e, 2 * ps + ph, hv, lv);
+          }
+        }
+      }
+      fence_proxy_async();         // V^T for the tensor cores; the raw buffer for the next copies
+      mbar_arrive(bar(kVFull, b));
+      staging_all(true);           // every staging thread is done with the raw buffer
+      if (st == 0 && ci + 2 < nck) issue(ci + 2);
+      issued = min(nck, ci + 3);
+    }
+    // after a wait that gave up, the copies still in flight land (bounded) before the CTA leaves
+    if (!ok)
+      for (int ci = consumed; ci < issued; ++ci) mbar_wait_bounded(bar(kRaw, ci & 1), (ci >> 1) & 1, p.status);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_f16_f32(kTileRows, NC);
+      constexpr uint32_t idesc_o = tc::idesc_f16_f32(kTileRows, D);
+      // S(i) = Q K(i)^T into score buffer i % 2, as soon as K(i) is staged and
+      // the softmax has read S(i - 2) there
+      auto mma_s = [&](int i) {
+        const int bb = i & 1, u = i >> 1;
+        ok = mbar_wait_bounded(bar(kKFull, bb), u & 1, p.status);
+        if (ok && i >= 2) ok = mbar_wait_bounded(bar(kSEmpty, bb), (u - 1) & 1, p.status);
+        if (!ok) return;
+        tc::fence_after_sync();
+        const uint32_t kbuf = sb + OFF_K + bb * 2 * KB;
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t a = tc::smem_desc(sb + OFF_Q + 256 * ks, 128, (D / 8) * 128);
+          tc::mma_f16(tmem + D + bb * NC, a, tc::smem_desc(kbuf + 256 * ks, 128, (D / 8) * 128), idesc_s, ks > 0);
+          if constexpr (kKLo)
+            tc::mma_f16(tmem + D + bb * NC, a, tc::smem_desc(kbuf + KB + 256 * ks, 128, (D / 8) * 128), idesc_s, 1);
+        }
+        tc::commit(bar(kKEmpty, bb));
+        tc::commit(bar(kSFull, bb));
+      };
+      // O += P(j) V(j) once the softmax has written P(j) and V(j) is staged
+      auto mma_o = [&](int j) {
+        const int bb = j & 1, u = j >> 1;
+        ok = mbar_wait_bounded(bar(kPFull, bb), u & 1, p.status);
+        if (ok) ok = mbar_wait_bounded(bar(kVFull, bb), u & 1, p.status);
+        if (!ok) return;
+        tc::fence_after_sync();
+        const uint32_t pbuf = sb + OFF_P + bb * PB, vbuf = sb + OFF_V + bb * 2 * VB;
+#pragma unroll 1
+        for (int ks = 0; ks < NC / 16; ++ks) {
+          const uint64_t a = tc::smem_desc(pbuf + 256 * ks, 128, (NC / 8) * 128);
+          tc::mma_f16(tmem, a, tc::smem_desc(vbuf + 256 * ks, 128, (NC / 8) * 128), idesc_o, j > 0 || ks > 0);
+          if constexpr (kVLo)
+            tc::mma_f16(tmem, a, tc::smem_desc(vbuf + VB + 256 * ks, 128, (NC / 8) * 128), idesc_o, 1);
+        }
+        tc::commit(bar(kVEmpty, bb));
+        tc::commit(bar(kPEmpty, bb));
+      };
+      // the scores run two chunks ahead of the output, so that the softmax of
+      // chunk j + 1 finds its scores ready while P(j) V(j) is computed
+      if (nck > 0) mma_s(0);
+      if (ok && nck > 1) mma_s(1);
+      for (int j = 0; j < nck && ok; ++j) {
+        mma_o(j);
+        if (ok && j + 2 < nck) mma_s(j + 2);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax --
+    const int rl = tid;                                   // row of the tile, tensor-memory lane
+    const uint32_t tlane = static_cast<uint32_t>(warp * 32) << 16;
+    float m_row = -INFINITY, l_row = 0.f;
+    for (int ci = 0; ci < nck && ok; ++ci) {
+      const int b = ci & 1, u = ci >> 1;
+      const uint32_t pmask = chunk_mask(ci);
+      ok = mbar_wait_bounded(bar(kSFull, b), u & 1, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t sr[NC];
+#pragma unroll
+      for (int k0 = 0; k0 < NC; k0 += 16) tc::ld_32x32b_x16(tmem + tlane + D + b * NC + k0, sr + k0);
+#pragma unroll
+      for (int k0 = 0; k0 < NC; k0 += 16) tc::wait_ld(sr + k0);
+      tc::fence_before_sync();
+      mbar_arrive(bar(kSEmpty, b));
+      float m_chunk = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        const bool valid = (pmask >> (k / kPage)) & 1u;
+        const float v = valid ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
+        sr[k] = __float_as_uint(v);
+        m_chunk = fmaxf(m_chunk, v);
+      }
+      float alpha = 1.f;
+      if (m_chunk > m_row + kLazy) {         // also the first chunk with a key (m_row = -inf)
+        if (m_row != -INFINITY) alpha = fast_exp2(m_row - m_chunk);
+        m_row = m_chunk;
+      }
+      if (ci > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O must be quiescent: the output MMA of the previous chunk is done
+        ok = mbar_wait_bounded(bar(kPEmpty, (ci - 1) & 1), ((ci - 1) >> 1) & 1, p.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int k0 = 0; k0 < D; k0 += 16) {
+          uint32_t orr[16];
+          tc::ld_32x32b_x16(tmem + tlane + k0, orr);
+          tc::wait_ld(orr);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+          tc::st_32x32b_x16(tmem + tlane + k0, orr);
+        }
+        tc::wait_st();
+      }
+      // P buffer ci % 2 is free once the output MMA of chunk ci - 2 is done
+      if (ci >= 2) ok = mbar_wait_bounded(bar(kPEmpty, b), (u - 1) & 1, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const uint32_t pbuf = sb + OFF_P + b * PB;
+      float lsum = 0.f;
+#pragma unroll
+      for (int g = 0; g < NC / 8; ++g) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = m_row == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[8 * g + 2 * e]) - m_row);
+          const float p1 = m_row == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[8 * g + 2 * e + 1]) - m_row);
+          const __half2 ph2 = __floats2half2_rn(p0, p1);
+          const float2 back = __half22float2(ph2);
+          lsum += back.x + back.y;
+          w4[e] = h2_bits(ph2);
+        }
+        sts128(pbuf + ((rl >> 3) * (NC / 8) + g) * 128 + (rl & 7) * 16, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+      }
+      l_row = l_row * alpha + lsum;
+      fence_proxy_async();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kPFull, b));
+    }
+    // the last output MMA done: o = O * v_post / l into padded rows (Q and the K^ buffers are free)
+    if (ok && nck > 0) ok = mbar_wait_bounded(bar(kPEmpty, (nck - 1) & 1), ((nck - 1) >> 1) & 1, p.status);
+    if (__all_sync(0xffffffffu, ok) && nck > 0) {
+      tc::fence_after_sync();
+      const float inv = l_row > 0.f ? p.v_post / l_row : 0.f;
+#pragma unroll 1
+      for (int k0 = 0; k0 < D; k0 += 32) {
+        uint32_t orr[32];
+        tc::ld_32x32b_x16(tmem + tlane + k0, orr);
+        tc::ld_32x32b_x16(tmem + tlane + k0 + 16, orr + 16);
+        tc::wait_ld(orr);
+        tc::wait_ld(orr + 16);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          sts128(sb + OFF_Q + rl * ROWB + (k0 + e) * 4,
+                 l_row > 0.f ? make_uint4(__float_as_uint(__uint_as_float(orr[e]) * inv),
+                                          __float_as_uint(__uint_as_float(orr[e + 1]) * inv),
+                                          __float_as_uint(__uint_as_float(orr[e + 2]) * inv),
+                                          __float_as_uint(__uint_as_float(orr[e + 3]) * inv))
+                             : make_uint4(0, 0, 0, 0));
+      }
+      xlse[rl] = l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
+    } else {
+      xlse[rl] = -INFINITY;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+
+  // cluster merge of the rows, as in the generic prefix pass (warps 0-7)
+  const int CL = p.cluster;
+  const uint32_t crank = cluster_ctarank();
+  const int part = blockIdx.x / CL;
+  const int rpc = kTileRows / CL;
+  cluster_sync();
+  if (warp < 8) {
+    for (int lr = static_cast<int>(crank) * rpc + warp; lr < (static_cast<int>(crank) + 1) * rpc; lr += 8) {
+      const int r = r0 + lr;
+      if (r >= rows) break;
+      float lsk[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        lsk[k] = k < CL ? ld_peer_f32(map_peer(smem_addr(xlse + lr), k)) : -INFINITY;
+        M = fmaxf(M, lsk[k]);
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w = lsk[k] == -INFINITY ? 0.f : fast_exp2(lsk[k] - M);
+        if (w == 0.f) continue;
+        L += w;
+        const float4 x = ld_peer_v4(map_peer(sb + OFF_Q + lr * ROWB, k) + 16 * lane);
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int bq = r / rows_per_seq, rem = r % rows_per_seq;
+      const size_t rowid = (static_cast<size_t>(bq) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
+                           rem % p.group;
+      reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_parts + part) * D)[lane] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (lane == 0) p.lse_pre[rowid * p.n_parts + part] = L > 0.f ? M + __log2f(L) : -INFINITY;
+    }
+  }
+  cluster_sync();
+
+  if (kvh == 0) {
+    const int b_first = r0 / rows_per_seq, b_last = (min(rows, r0 + kTileRows) - 1) / rows_per_seq;
+    const int pages = nck * NPG;
+    for (int i = tid; i < (b_last - b_first + 1) * pages; i += kWsThreads) {
+      const int bb = b_first + i / pages, j = c0 * NPG + i % pages;
+      if (j * kPage < p.prefix_len && p.page_table[static_cast<size_t>(bb) * p.max_pages + j] != p.page_table[j])
+        flag_error(p.status, MEMRA_DEVERR_PREFIX);
+    }
+    if (blockIdx.x == 0)
+      for (int bb = b_first + tid; bb <= b_last; bb += kWsThreads)
+        if (p.seq_lens[bb] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TCOLS);
+}
+
 // Merge of a row's prefix-chunk partials and its own-key split partials.
 template <int D>
 __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const CascadeCombineParams p) {
@@ -795,16 +1306,26 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
   }
 }
 
+// The prefix-pass kernel of a head_dim: warp-specialized at 128, generic at 256.
+template <int D, int KF, int VF>
+constexpr auto prefix_kernel() {
+  if constexpr (D == 128)
+    return cascade_prefix_ws_kernel<KF, VF>;
+  else
+    return cascade_prefix_kernel<D, KF, VF>;
+}
+
 template <int D, int KF, int VF>
 cudaError_t wave_one(int *cluster, int *wave_ctas) {
   constexpr uint32_t smem_max = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), kCascadeMaxChunksPerCta);
   // any mix of prefix-pass CTAs that fits an SM by shared memory fits its tensor memory
   constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128, 1) + 1024u;   // smallest CTAs
   constexpr uint32_t kMin256 = cascade_smem_bytes(256, 9 * 256, 9 * 256, 1) + 1024u;
-  static_assert(3u * kMin128 > 233472u && 2u * cascade_tmem_cols(128) <= 512u, "two 128s at most");
-  static_assert(2u * kMin256 > 233472u && kMin256 + kMin128 > 233472u && cascade_tmem_cols(256) <= 512u,
-                "one 256 and nothing else");
-  auto kernel = cascade_prefix_kernel<D, KF, VF>;
+  static_assert(2u * kMin128 > 233472u && 2u * kMin256 > 233472u && kMin256 + kMin128 > 233472u &&
+                    cascade_tmem_cols(128) <= 512u && cascade_tmem_cols(256) <= 512u,
+                "one prefix-pass CTA per SM, whatever the head_dim");
+  constexpr int kT = D == 128 ? kWsThreads : kThreads;
+  auto kernel = prefix_kernel<D, KF, VF>();
   // Per device and instantiation, for the largest footprint (a CTA that loops):
   // the cluster size, the largest of 8, 4, 2 whose co-resident clusters place
   // at least 90% of the CTAs that single CTAs would (on 152 SMs, clusters of 8
@@ -832,7 +1353,7 @@ cudaError_t wave_one(int *cluster, int *wave_ctas) {
     auto active = [&](int cl) {      // co-resident clusters of cl CTAs, as the occupancy query counts them
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
-      cfg.blockDim = dim3(kThreads);
+      cfg.blockDim = dim3(kT);
       cfg.dynamicSmemBytes = smem_max;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -873,7 +1394,7 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   cudaError_t e = wave_one<D, KF, VF>(&cl, &wave);     // also sets the shared-memory limit once
   if (e != cudaSuccess) return e;
   const uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), p.cpc);
-  auto kernel = cascade_prefix_kernel<D, KF, VF>;
+  auto kernel = prefix_kernel<D, KF, VF>();
   const int n_ctas = (p.n_chunks + p.cpc - 1) / p.cpc;      // CTAs per (KV head, row tile)
   while (cl > 1 && cl > n_ctas) cl /= 2;
   p.cluster = cl;
@@ -882,7 +1403,7 @@ cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.n_parts * cl), static_cast<unsigned>(p.n_kv_heads),
                      static_cast<unsigned>((rows + kTileRows - 1) / kTileRows));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(D == 128 ? kWsThreads : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

@@ -12,10 +12,11 @@
 
 namespace memra {
 
-// Prefix tokens one CTA of the prefix pass covers (the N of its score MMA),
-// and its CTAs per SM (registers and shared memory allow two at head_dim 128).
+// Prefix tokens of one chunk (the N of the score MMA), and prefix-pass CTAs
+// per SM: one either way (the warp-specialized head_dim 128 pass fills the
+// SM's shared memory; the head_dim 256 pass needs more than half of it).
 __host__ __device__ constexpr int cascade_chunk_tokens(int D) { return D == 128 ? 64 : 64; }
-__host__ __device__ constexpr int cascade_ctas_per_sm(int D) { return D == 128 ? 2 : 1; }
+__host__ __device__ constexpr int cascade_ctas_per_sm(int D) { return D == 128 ? 1 : 1; }
 
 struct CascadeParams {
   const uint8_t *k_pool;
@@ -53,29 +54,34 @@ constexpr int kCascadeMaxChunksPerCta = 64;
 // bytes and cpc chunks per CTA: the Q tile, one half-chunk of K^ and of V^T
 // (hi and lo parts), the raw pages (two buffers when the CTA loops), the
 // softmax exchange, the page ids, the barriers.
-// At head_dim 256 the request is at least 155 KiB, so that no head_dim-128 CTA
-// (and its tensor memory) fits beside it.
+// At head_dim 256 the request is at least 155 KiB, so that no other prefix-pass
+// CTA (and its tensor memory) fits beside it.  At head_dim 128 (the
+// warp-specialized pass): the Q tile, two K^ and two V^T chunk buffers (hi and
+// lo parts), two P buffers, two raw page buffers, the row lse, the page ids,
+// the barriers.
 __host__ __device__ constexpr uint32_t cascade_smem_plan(int D, int kseg, int vseg, int cpc) {
-  return 128u * D * 2 + 2u * cascade_chunk_tokens(D) * D * 2 +
-         (cpc > 1 ? 2u : 1u) * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) +
-         5u * 128u * 4u + 4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 64u;
+  return D == 128
+             ? 128u * D * 2 + 8u * cascade_chunk_tokens(D) * D * 2 + 2u * 128u * cascade_chunk_tokens(D) * 2 +
+                   2u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 128u * 4u +
+                   4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 192u
+             : 128u * D * 2 + 2u * cascade_chunk_tokens(D) * D * 2 +
+                   (cpc > 1 ? 2u : 1u) * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) *
+                       (kseg + vseg) +
+                   5u * 128u * 4u + 4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 64u;
 }
 __host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg, int cpc) {
   return D == 256 && cascade_smem_plan(D, kseg, vseg, cpc) < 155u * 1024u ? 155u * 1024u
                                                                            : cascade_smem_plan(D, kseg, vseg, cpc);
 }
 
-// Tensor-memory columns of one prefix-pass CTA: O (head_dim columns) and the
-// chunk's scores S, rounded up to a power of two (256 at head_dim 128, 512 at
-// 256).  The hardware places CTAs, and whole clusters, by registers and shared
+// Tensor-memory columns of one prefix-pass CTA, a power of two: at head_dim
+// 128, O and two score buffers (256); at 256, O and one score buffer (512).
+// The hardware places CTAs, and whole clusters, by registers and shared
 // memory, not by tensor memory, so any mix of prefix-pass CTAs that fits an SM
-// by shared memory must fit its 512 columns: two of head_dim 128 (>= 76 KB
-// each, so never three) or one of head_dim 256 (>= 148 KB, with no room for a
-// 128 beside it).  A CTA that found the columns taken would wait in its
-// allocation while its cluster peers wait for it.
-__host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) {
-  return D + cascade_chunk_tokens(D) <= 256 ? 256u : 512u;
-}
+// by shared memory must fit its 512 columns: here, one CTA of either kind
+// (>= 205 KB and >= 155 KB).  A CTA that found the columns taken would wait
+// in its allocation while its cluster peers wait for it.
+__host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) { return D == 128 ? 256u : 512u; }
 
 // The prefix pass's cluster size on this device for these formats and the
 // CTAs one wave of it holds (both independent of the batch).
