@@ -199,15 +199,17 @@ int check_decode(const DecodeArgs &a) {
 }
 
 // Chunks per prefix-pass CTA of a cascade call: few enough CTAs per KV head
-// that one row tile's fit one wave of the pass (as the device co-schedules its
-// clusters), never more than kCascadeMaxChunksPerCta chunks each.  Depends on
-// the prefix, head_dim, formats, KV heads and the device only.
+// that one row tile's fit one wave of the pass, at least
+// kCascadeMinChunksPerCta and never more than kCascadeMaxChunksPerCta chunks
+// each.  Depends on the prefix, head_dim, formats, KV heads and the device
+// only.
 int cascade_cpc(int32_t prefix, int32_t head_dim, int kf, int vf, int32_t n_kv_heads, int *cpc) {
-  int cl = 1, wave = 1;
-  if (cascade_wave(head_dim, kf, vf, &cl, &wave) != cudaSuccess) return MEMRA_ERR_CUDA;
+  int wave = 1;
+  if (cascade_wave(head_dim, kf, vf, &wave) != cudaSuccess) return MEMRA_ERR_CUDA;
   const int64_t n_chunks = ceil_div(prefix, cascade_chunk_tokens(head_dim));
   const int64_t target = std::max<int64_t>(1, wave / n_kv_heads);
-  *cpc = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(n_chunks, target), 1),
+  const int64_t floor = std::min<int64_t>(kCascadeMinChunksPerCta, std::max<int64_t>(n_chunks, 1));
+  *cpc = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(n_chunks, target), floor),
                                             kCascadeMaxChunksPerCta));
   return MEMRA_OK;
 }

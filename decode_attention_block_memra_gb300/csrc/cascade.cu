@@ -63,35 +63,25 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr) {
   return v;
 }
 
-// Thread-block clusters: this CTA's rank, a barrier over every thread of the
-// cluster (release / acquire), and loads from a peer CTA's shared memory.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+// One thread: copy `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from shared to global memory through the async proxy, as one bulk
+// async-group of this thread.
+__device__ __forceinline__ void bulk_store_s2g(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// One thread: its bulk stores have completed, writes performed (before the
+// CTA, and its shared memory, goes away).
+__device__ __forceinline__ void bulk_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr) : "memory");
-  return v;
+// Global row id of row r of a KV head's row tiles: sequence b = r / (q_len *
+// group), then query position and head of the group.
+__device__ __forceinline__ size_t prefix_row_id(const CascadeParams &p, int kvh, int r) {
+  const int rows_per_seq = p.q_len * p.group;
+  const int b = r / rows_per_seq, rem = r % rows_per_seq;
+  return (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group + rem % p.group;
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
@@ -251,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   // rows) and P after the scores; one half of V^T (hi, lo; dim rows); two
   // buffers of raw pages (a chunk's K pages, then its V pages), the next
   // chunk's copies landing in one while the other is staged; the softmax
-  // exchange and row lse; the page ids of the CTA's chunks; barriers.  The
-  // output rows reuse Q, K^, V^T and the raw buffers once O is done.
+  // exchange; the page ids of the CTA's chunks; barriers.  The output rows
+  // reuse Q, K^, V^T and the raw buffers once O is done.
   constexpr uint32_t QB = kTileRows * D * 2, KHB = H * D * 2, VHB = D * H * 2;
   constexpr uint32_t RAWB = NPG * (KSEG + VSEG);
   constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 2 * KHB, OFF_RAW = OFF_V + 2 * VHB;
@@ -260,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   constexpr uint32_t TCOLS = cascade_tmem_cols(D);            // O at column 0, S at column D
   // one raw buffer when the CTA has one chunk, two when it loops over several
   const uint32_t nbuf = p.cpc > 1 ? 2u : 1u;
-  const uint32_t OFF_X = OFF_RAW + nbuf * RAWB, OFF_PID = OFF_X + 5 * kTileRows * 4,
+  const uint32_t OFF_X = OFF_RAW + nbuf * RAWB, OFF_PID = OFF_X + 4 * kTileRows * 4,
                  OFF_BAR = OFF_PID + 4 * NPG * p.cpc;
-  static_assert(OFF_RAW + 2 * RAWB + 5 * kTileRows * 4 + 4 * NPG * kCascadeMaxChunksPerCta + 64 ==
+  static_assert(OFF_RAW + 2 * RAWB + 4 * kTileRows * 4 + 4 * NPG * kCascadeMaxChunksPerCta + 64 ==
                     cascade_smem_plan(D, KSEG, VSEG, kCascadeMaxChunksPerCta) &&
-                    OFF_RAW + RAWB + 5 * kTileRows * 4 + 4 * NPG + 64 == cascade_smem_plan(D, KSEG, VSEG, 1),
+                    OFF_RAW + RAWB + 4 * kTileRows * 4 + 4 * NPG + 64 == cascade_smem_plan(D, KSEG, VSEG, 1),
                 "shared-memory plan");
   static_assert(cascade_smem_bytes(D, KSEG, VSEG, kCascadeMaxChunksPerCta) <= kSmemLimit, "shared memory");
   static_assert(kTileRows * ROWB <= OFF_RAW + RAWB, "output rows below the exchange");
@@ -287,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   int *pid_s = reinterpret_cast<int *>(smem + OFF_PID);        // [chunk of the CTA][page], -1 = none
   float *xm = reinterpret_cast<float *>(smem + OFF_X);
   float *xl = xm + 2 * kTileRows;
-  float *xlse = xl + 2 * kTileRows;
 
   const int kvh = blockIdx.y;
   const int rows = p.batch * p.q_len * p.group;                  // query rows of one KV head
@@ -638,58 +627,18 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
                            : make_uint4(0, 0, 0, 0));
     }
   }
-  if (colh == 0) xlse[rl] = ok && nck > 0 && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
-
-  // The CTAs of a cluster hold consecutive chunk ranges of the same rows: CTA
-  // rank c merges rows c * 128/CL .. of every CTA's shared memory (log-sum-exp)
-  // and writes one partial per row for the cluster, with coalesced stores.  The
-  // second cluster barrier keeps each CTA's rows in place until its peers have
-  // read them.
-  const int CL = p.cluster;
-  const uint32_t crank = cluster_ctarank();
-  const int part = blockIdx.x / CL;
-  const int rpc = kTileRows / CL;
-  cluster_sync();
-  for (int lr = static_cast<int>(crank) * rpc + warp; lr < (static_cast<int>(crank) + 1) * rpc; lr += kThreads / 32) {
-    const int r = r0 + lr;
-    if (r >= rows) break;
-    float lsk[8];
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      lsk[k] = k < CL ? ld_peer_f32(map_peer(smem_addr(xlse + lr), k)) : -INFINITY;
-      M = fmaxf(M, lsk[k]);
-    }
-    float4 acc[D / 128];
-#pragma unroll
-    for (int q = 0; q < D / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float w = lsk[k] == -INFINITY ? 0.f : fast_exp2(lsk[k] - M);
-      if (w == 0.f) continue;              // no key there (or a peer that gave up): never read
-      L += w;
-      const uint32_t row = map_peer(sb + OFF_Q + lr * ROWB, k);
-#pragma unroll
-      for (int q = 0; q < D / 128; ++q) {
-        const float4 x = ld_peer_v4(row + 16 * (lane + 32 * q));
-        acc[q].x = fmaf(w, x.x, acc[q].x);
-        acc[q].y = fmaf(w, x.y, acc[q].y);
-        acc[q].z = fmaf(w, x.z, acc[q].z);
-        acc[q].w = fmaf(w, x.w, acc[q].w);
-      }
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int b = r / rows_per_seq, rem = r % rows_per_seq;
-    const size_t rowid = (static_cast<size_t>(b) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
-                         rem % p.group;
-    float4 *dst = reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_parts + part) * D);
-#pragma unroll
-    for (int q = 0; q < D / 128; ++q)
-      dst[lane + 32 * q] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
-    if (lane == 0) p.lse_pre[rowid * p.n_parts + part] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  // This CTA's partial of each row: the row by one bulk copy of its padded
+  // shared-memory row (both column halves, ordered for the async proxy by the
+  // fence and the barrier), the lse by a plain store.  A row without keys, or
+  // every row after a wait that gave up, gets lse = -inf, which the merge
+  // never weighs.
+  fence_proxy_async();
+  __syncthreads();
+  if (colh == 0 && r0 + rl < rows) {
+    const size_t slot = prefix_row_id(p, kvh, r0 + rl) * p.n_parts + blockIdx.x;
+    if (ok && nck > 0) bulk_store_s2g(p.o_pre + slot * D, sb + OFF_Q + rl * ROWB, D * 4);
+    p.lse_pre[slot] = ok && nck > 0 && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
   }
-  cluster_sync();
 
   // Every sequence of the row tile must hold the same prefix pages and see all
   // of the prefix (flags only, off the critical path; one KV head checks).
@@ -711,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, cascade_ctas_per_sm(D)) cascade_pref
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
+  bulk_store_wait();               // the row copies this thread issued (none: returns at once)
 }
 
 // Warps of the warp-specialized pass: 4 softmax, kStageWarps staging, 1 MMA.
@@ -761,12 +711,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
   constexpr bool kVLo = VF == MEMRA_KV_Q5_1 || VF == MEMRA_KV_Q4_0;
   constexpr float kLazy = 8.f;                      // log2 units: P stays <= 256 between rescales
   // Shared memory: Q tile | K^ buffers [2] (hi, lo) | V^T buffers [2] (hi, lo)
-  // | P buffers [2] | raw page buffers [2] | row lse | page ids | barriers.
+  // | P buffers [2] | raw page buffers [2] | page ids | barriers.
   // The output rows reuse Q and the K^ buffers once the last MMA is done.
   constexpr uint32_t QB = kTileRows * D * 2, KB = NC * D * 2, VB = D * NC * 2, PB = kTileRows * NC * 2;
   constexpr uint32_t RAWB = NPG * (KSEG + VSEG);
   constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + 4 * KB, OFF_P = OFF_V + 4 * VB, OFF_RAW = OFF_P + 2 * PB,
-                     OFF_X = OFF_RAW + 2 * RAWB, OFF_PID = OFF_X + kTileRows * 4;
+                     OFF_PID = OFF_RAW + 2 * RAWB;
   constexpr uint32_t ROWB = D * 4 + 16;
   constexpr uint32_t TCOLS = cascade_tmem_cols(D);
   static_assert(OFF_PID + 4 * NPG * kCascadeMaxChunksPerCta + 192 ==
@@ -793,7 +743,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
   enum { kRaw = 0, kKFull, kKEmpty, kVFull, kVEmpty, kSFull, kSEmpty, kPFull, kPEmpty };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 16 * 9);
   int *pid_s = reinterpret_cast<int *>(smem + OFF_PID);
-  float *xlse = reinterpret_cast<float *>(smem + OFF_X);
 
   const int kvh = blockIdx.y;
   const int rows = p.batch * p.q_len * p.group;
@@ -1006,6 +955,21 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
     // after a wait that gave up, the copies still in flight land (bounded) before the CTA leaves
     if (!ok)
       for (int ci = consumed; ci < issued; ++ci) mbar_wait_bounded(bar(kRaw, ci & 1), (ci >> 1) & 1, p.status);
+    // Every sequence of the row tile must hold the same prefix pages and see
+    // all of the prefix.  Checked here, while the last chunk's MMAs and softmax
+    // are still running (flags only; one KV head checks).
+    if (kvh == 0) {
+      const int b_first = r0 / rows_per_seq, b_last = (min(rows, r0 + kTileRows) - 1) / rows_per_seq;
+      const int pages = nck * NPG;
+      for (int i = st; i < (b_last - b_first + 1) * pages; i += kStageThreads) {
+        const int bb = b_first + i / pages, j = c0 * NPG + i % pages;
+        if (j * kPage < p.prefix_len && p.page_table[static_cast<size_t>(bb) * p.max_pages + j] != p.page_table[j])
+          flag_error(p.status, MEMRA_DEVERR_PREFIX);
+      }
+      if (blockIdx.x == 0)
+        for (int bb = b_first + st; bb <= b_last; bb += kStageThreads)
+          if (p.seq_lens[bb] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
+    }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
@@ -1139,6 +1103,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
     }
     // the last output MMA done: o = O * v_post / l into padded rows (Q and the K^ buffers are free)
     if (ok && nck > 0) ok = mbar_wait_bounded(bar(kPEmpty, (nck - 1) & 1), ((nck - 1) >> 1) & 1, p.status);
+    bool wrote = false;
     if (__all_sync(0xffffffffu, ok) && nck > 0) {
       tc::fence_after_sync();
       const float inv = l_row > 0.f ? p.v_post / l_row : 0.f;
@@ -1158,70 +1123,25 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
                                           __float_as_uint(__uint_as_float(orr[e + 3]) * inv))
                              : make_uint4(0, 0, 0, 0));
       }
-      xlse[rl] = l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
-    } else {
-      xlse[rl] = -INFINITY;
+      wrote = true;
     }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-
-  // cluster merge of the rows, as in the generic prefix pass (warps 0-7)
-  const int CL = p.cluster;
-  const uint32_t crank = cluster_ctarank();
-  const int part = blockIdx.x / CL;
-  const int rpc = kTileRows / CL;
-  cluster_sync();
-  if (warp < 8) {
-    for (int lr = static_cast<int>(crank) * rpc + warp; lr < (static_cast<int>(crank) + 1) * rpc; lr += 8) {
-      const int r = r0 + lr;
-      if (r >= rows) break;
-      float lsk[8];
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        lsk[k] = k < CL ? ld_peer_f32(map_peer(smem_addr(xlse + lr), k)) : -INFINITY;
-        M = fmaxf(M, lsk[k]);
+    // This CTA's partial of the row: the row by one bulk copy of the padded
+    // shared-memory row this thread wrote, the lse by a plain store.  A row
+    // without keys, or every row after a wait that gave up, gets lse = -inf,
+    // which the merge never weighs.
+    if (r0 + rl < rows) {
+      const size_t slot = prefix_row_id(p, kvh, r0 + rl) * p.n_parts + blockIdx.x;
+      if (wrote) {
+        fence_proxy_async();
+        bulk_store_s2g(p.o_pre + slot * D, sb + OFF_Q + rl * ROWB, D * 4);
       }
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float L = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float w = lsk[k] == -INFINITY ? 0.f : fast_exp2(lsk[k] - M);
-        if (w == 0.f) continue;
-        L += w;
-        const float4 x = ld_peer_v4(map_peer(sb + OFF_Q + lr * ROWB, k) + 16 * lane);
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const int bq = r / rows_per_seq, rem = r % rows_per_seq;
-      const size_t rowid = (static_cast<size_t>(bq) * p.q_len + rem / p.group) * p.n_heads + kvh * p.group +
-                           rem % p.group;
-      reinterpret_cast<float4 *>(p.o_pre + (rowid * p.n_parts + part) * D)[lane] =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      if (lane == 0) p.lse_pre[rowid * p.n_parts + part] = L > 0.f ? M + __log2f(L) : -INFINITY;
+      p.lse_pre[slot] = wrote && l_row > 0.f ? m_row + __log2f(l_row) : -INFINITY;
     }
-  }
-  cluster_sync();
-
-  if (kvh == 0) {
-    const int b_first = r0 / rows_per_seq, b_last = (min(rows, r0 + kTileRows) - 1) / rows_per_seq;
-    const int pages = nck * NPG;
-    for (int i = tid; i < (b_last - b_first + 1) * pages; i += kWsThreads) {
-      const int bb = b_first + i / pages, j = c0 * NPG + i % pages;
-      if (j * kPage < p.prefix_len && p.page_table[static_cast<size_t>(bb) * p.max_pages + j] != p.page_table[j])
-        flag_error(p.status, MEMRA_DEVERR_PREFIX);
-    }
-    if (blockIdx.x == 0)
-      for (int bb = b_first + tid; bb <= b_last; bb += kWsThreads)
-        if (p.seq_lens[bb] - p.q_len < p.prefix_len) flag_error(p.status, MEMRA_DEVERR_BAD_SEQ_LEN);
   }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TCOLS);
+  bulk_store_wait();               // the row copies this thread issued (none: returns at once)
 }
 
 // Merge of a row's prefix-chunk partials and its own-key split partials.
@@ -1276,7 +1196,10 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
       }
 #pragma unroll
       for (int u = 0; u < BATCH; ++u) {
-        const float wgt = ls[u] == -INFINITY ? 0.f : fast_exp2(ls[u] - M);
+        // a part with lse = -inf (no keys, or a CTA that gave up) is never
+        // weighed: its row may hold anything
+        if (ls[u] == -INFINITY) continue;
+        const float wgt = fast_exp2(ls[u] - M);
         L += wgt;
 #pragma unroll
         for (int q4 = 0; q4 < PER / 4; ++q4) {
@@ -1316,7 +1239,7 @@ constexpr auto prefix_kernel() {
 }
 
 template <int D, int KF, int VF>
-cudaError_t wave_one(int *cluster, int *wave_ctas) {
+cudaError_t wave_one(int *wave_ctas) {
   constexpr uint32_t smem_max = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), kCascadeMaxChunksPerCta);
   // any mix of prefix-pass CTAs that fits an SM by shared memory fits its tensor memory
   constexpr uint32_t kMin128 = cascade_smem_bytes(128, 9 * 128, 9 * 128, 1) + 1024u;   // smallest CTAs
@@ -1324,110 +1247,62 @@ cudaError_t wave_one(int *cluster, int *wave_ctas) {
   static_assert(2u * kMin128 > 233472u && 2u * kMin256 > 233472u && kMin256 + kMin128 > 233472u &&
                     cascade_tmem_cols(128) <= 512u && cascade_tmem_cols(256) <= 512u,
                 "one prefix-pass CTA per SM, whatever the head_dim");
-  constexpr int kT = D == 128 ? kWsThreads : kThreads;
   auto kernel = prefix_kernel<D, KF, VF>();
-  // Per device and instantiation, for the largest footprint (a CTA that loops):
-  // the cluster size, the largest of 8, 4, 2 whose co-resident clusters place
-  // at least 90% of the CTAs that single CTAs would (on 152 SMs, clusters of 8
-  // of these CTAs fit only 15 at a time), else 1; and the CTAs one wave holds.
-  // The wave is the SMs times the CTAs per SM the kernel is built for (two at
-  // head_dim 128: registers, shared memory and tensor memory allow it, and
-  // traces show them co-resident), scaled by that cluster fraction; the
-  // occupancy query itself reports one CTA per SM for this kernel.  Both depend
-  // on the device and the formats only, never on the batch.
-  static int widest[64] = {}, wave[64] = {};
+  // Per device and instantiation: the CTAs one wave holds, the SMs times the
+  // CTAs per SM the kernel is built for (one).  It depends on the device only,
+  // never on the batch.  The kernel's shared-memory limit is set here once.
+  static int wave[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!widest[dev]) {
+  if (!wave[dev]) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
     if (e != cudaSuccess) return e;
-    // all of the SM's unified L1 / shared memory as shared memory, so that two
-    // CTAs of ~100 KB share an SM
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    auto active = [&](int cl) {      // co-resident clusters of cl CTAs, as the occupancy query counts them
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
-      cfg.blockDim = dim3(kT);
-      cfg.dynamicSmemBytes = smem_max;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-        cudaGetLastError();          // a refused query is not an error of this call
-        n = 0;
-      }
-      return n;
-    };
-    const int single = active(1);
-    const int slots = sms * cascade_ctas_per_sm(D);
-    int w = 1, ctas = slots;
-    for (int cl = 8; cl > 1 && single > 0; cl /= 2) {
-      const int n = active(cl);
-      if (10 * n * cl >= 9 * single) {
-        w = cl;
-        ctas = static_cast<int>(static_cast<int64_t>(slots) * n * cl / single);
-        break;
-      }
-    }
-    wave[dev] = ctas > 0 ? ctas : 1;
-    widest[dev] = w;
+    wave[dev] = std::max(1, sms * cascade_ctas_per_sm(D));
   }
-  *cluster = widest[dev];
   *wave_ctas = wave[dev];
   return cudaSuccess;
 }
 
 template <int D, int KF, int VF>
 cudaError_t launch_prefix_one(CascadeParams &p, cudaStream_t st) {
-  int cl = 1, wave = 1;
-  cudaError_t e = wave_one<D, KF, VF>(&cl, &wave);     // also sets the shared-memory limit once
+  int wave = 1;
+  cudaError_t e = wave_one<D, KF, VF>(&wave);     // also sets the shared-memory limit once
   if (e != cudaSuccess) return e;
   const uint32_t smem = cascade_smem_bytes(D, k_seg_bytes(KF, D), v_seg_bytes(VF, D), p.cpc);
   auto kernel = prefix_kernel<D, KF, VF>();
-  const int n_ctas = (p.n_chunks + p.cpc - 1) / p.cpc;      // CTAs per (KV head, row tile)
-  while (cl > 1 && cl > n_ctas) cl /= 2;
-  p.cluster = cl;
-  p.n_parts = (n_ctas + cl - 1) / cl;
+  p.n_parts = (p.n_chunks + p.cpc - 1) / p.cpc;      // CTAs per (KV head, row tile): one partial each
   const int rows = p.batch * p.q_len * p.group;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_parts * cl), static_cast<unsigned>(p.n_kv_heads),
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_parts), static_cast<unsigned>(p.n_kv_heads),
                      static_cast<unsigned>((rows + kTileRows - 1) / kTileRows));
   cfg.blockDim = dim3(D == 128 ? kWsThreads : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   const CascadeParams args = p;
   return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 template <int D>
-cudaError_t wave_formats(int kf, int vf, int *cluster, int *wave_ctas) {
+cudaError_t wave_formats(int kf, int vf, int *wave_ctas) {
   auto by_v = [&](auto kc) -> cudaError_t {
     constexpr int K = decltype(kc)::value;
     switch (vf) {
-      case MEMRA_KV_Q5_1: return wave_one<D, K, MEMRA_KV_Q5_1>(cluster, wave_ctas);
-      case MEMRA_KV_Q4_0: return wave_one<D, K, MEMRA_KV_Q4_0>(cluster, wave_ctas);
-      case MEMRA_KV_FP8_E4M3: return wave_one<D, K, MEMRA_KV_FP8_E4M3>(cluster, wave_ctas);
-      case MEMRA_KV_NVFP4: return wave_one<D, K, MEMRA_KV_NVFP4>(cluster, wave_ctas);
+      case MEMRA_KV_Q5_1: return wave_one<D, K, MEMRA_KV_Q5_1>(wave_ctas);
+      case MEMRA_KV_Q4_0: return wave_one<D, K, MEMRA_KV_Q4_0>(wave_ctas);
+      case MEMRA_KV_FP8_E4M3: return wave_one<D, K, MEMRA_KV_FP8_E4M3>(wave_ctas);
+      case MEMRA_KV_NVFP4: return wave_one<D, K, MEMRA_KV_NVFP4>(wave_ctas);
       default: return cudaErrorInvalidValue;
     }
   };
@@ -1466,8 +1341,8 @@ cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaS
   return D == 128 ? prefix_formats<128>(kf, vf, p, st) : prefix_formats<256>(kf, vf, p, st);
 }
 
-cudaError_t cascade_wave(int D, int kf, int vf, int *cluster, int *wave_ctas) {
-  return D == 128 ? wave_formats<128>(kf, vf, cluster, wave_ctas) : wave_formats<256>(kf, vf, cluster, wave_ctas);
+cudaError_t cascade_wave(int D, int kf, int vf, int *wave_ctas) {
+  return D == 128 ? wave_formats<128>(kf, vf, wave_ctas) : wave_formats<256>(kf, vf, wave_ctas);
 }
 
 cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st) {

@@ -29,8 +29,7 @@ struct CascadeParams {
   float *lse_pre;     // [batch * q_len * n_heads][n_parts]
   int batch, q_len, n_heads, group, n_kv_heads, num_pages, max_pages, prefix_len, n_chunks;
   int cpc;            // chunks per CTA (1 .. kCascadeMaxChunksPerCta)
-  int cluster;        // CTAs per cluster along the chunks (1, 2, 4 or 8), set by the launcher
-  int n_parts;        // prefix partials per row: ceil(CTAs per row tile / cluster), set by the launcher
+  int n_parts;        // prefix partials per row: the CTAs per (KV head, row tile), set by the launcher
   float scale_log2;   // sm_scale * (post-scale of the staged K values) * log2(e)
   float v_post;       // post-scale of the staged V values
 };
@@ -47,8 +46,13 @@ struct CascadeCombineParams {
   int n_parts;            // prefix partials per row (CascadeParams::n_parts of the prefix pass)
 };
 
-// Chunks one prefix-pass CTA loops over at most.
+// Chunks one prefix-pass CTA loops over at most, and at least (unless the
+// prefix is shorter).  The floor keeps a CTA's fixed costs (page ids, the Q
+// tile, the first copies, the output rows) to a fraction of its time, and on
+// a short prefix it leaves SMs free for the call's own-key pass, which then
+// runs beside the prefix pass instead of after it.
 constexpr int kCascadeMaxChunksPerCta = 64;
+constexpr int kCascadeMinChunksPerCta = 3;
 
 // Shared memory of one prefix-pass CTA for head_dim D, the formats' segment
 // bytes and cpc chunks per CTA: the Q tile, one half-chunk of K^ and of V^T
@@ -57,17 +61,16 @@ constexpr int kCascadeMaxChunksPerCta = 64;
 // At head_dim 256 the request is at least 155 KiB, so that no other prefix-pass
 // CTA (and its tensor memory) fits beside it.  At head_dim 128 (the
 // warp-specialized pass): the Q tile, two K^ and two V^T chunk buffers (hi and
-// lo parts), two P buffers, two raw page buffers, the row lse, the page ids,
-// the barriers.
+// lo parts), two P buffers, two raw page buffers, the page ids, the barriers.
 __host__ __device__ constexpr uint32_t cascade_smem_plan(int D, int kseg, int vseg, int cpc) {
   return D == 128
              ? 128u * D * 2 + 8u * cascade_chunk_tokens(D) * D * 2 + 2u * 128u * cascade_chunk_tokens(D) * 2 +
-                   2u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) + 128u * 4u +
+                   2u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * (kseg + vseg) +
                    4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 192u
              : 128u * D * 2 + 2u * cascade_chunk_tokens(D) * D * 2 +
                    (cpc > 1 ? 2u : 1u) * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) *
                        (kseg + vseg) +
-                   5u * 128u * 4u + 4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 64u;
+                   4u * 128u * 4u + 4u * static_cast<uint32_t>(cascade_chunk_tokens(D) / MEMRA_PAGE_SIZE) * cpc + 64u;
 }
 __host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int vseg, int cpc) {
   return D == 256 && cascade_smem_plan(D, kseg, vseg, cpc) < 155u * 1024u ? 155u * 1024u
@@ -76,19 +79,17 @@ __host__ __device__ constexpr uint32_t cascade_smem_bytes(int D, int kseg, int v
 
 // Tensor-memory columns of one prefix-pass CTA, a power of two: at head_dim
 // 128, O and two score buffers (256); at 256, O and one score buffer (512).
-// The hardware places CTAs, and whole clusters, by registers and shared
-// memory, not by tensor memory, so any mix of prefix-pass CTAs that fits an SM
-// by shared memory must fit its 512 columns: here, one CTA of either kind
-// (>= 205 KB and >= 155 KB).  A CTA that found the columns taken would wait
-// in its allocation while its cluster peers wait for it.
+// The hardware places CTAs by registers and shared memory, not by tensor
+// memory, so any mix of prefix-pass CTAs that fits an SM by shared memory
+// must fit its 512 columns: here, one CTA of either kind (>= 205 KB and >=
+// 155 KB).  A CTA that found the columns taken would wait in its allocation.
 __host__ __device__ constexpr uint32_t cascade_tmem_cols(int D) { return D == 128 ? 256u : 512u; }
 
-// The prefix pass's cluster size on this device for these formats and the
-// CTAs one wave of it holds (both independent of the batch).
-cudaError_t cascade_wave(int D, int kf, int vf, int *cluster, int *wave_ctas);
+// The CTAs one wave of the prefix pass holds on this device (independent of
+// the batch).
+cudaError_t cascade_wave(int D, int kf, int vf, int *wave_ctas);
 
-// Narrows the cluster size to the CTAs per row tile, fills p.cluster and
-// p.n_parts, and launches.
+// Fills p.n_parts (one partial per CTA of a row tile) and launches.
 cudaError_t launch_cascade_prefix(int D, int kf, int vf, CascadeParams &p, cudaStream_t st);
 cudaError_t launch_cascade_combine(int D, const CascadeCombineParams &p, cudaStream_t st);
 

@@ -195,9 +195,12 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   // Inputs written by the launch before this one have landed.  A cascade
   // call's own-key pass (skip > 0) runs beside the prefix pass launched just
   // before it instead: it reads nothing that pass writes, and the call's
-  // inputs were complete before that pass let it start.  It waits for that
-  // pass at its end, so that the merge after it sees both.
+  // inputs were complete before that pass let it start.  One of its CTAs waits
+  // for that pass before leaving, so this grid completes after it and the
+  // merge launched after this grid sees both; the other CTAs leave as soon as
+  // they are done and free their SM for the rest of the grid.
   if (p.skip == 0) grid_dependency_wait();
+  const bool waits_for_prefix = p.skip != 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   // This CTA: query position qi of sequence b and query heads 8 hg .. 8 hg + 7
   // of KV head kvh's group, over the keys visible to position qi (the first
@@ -211,7 +214,10 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
                                  blockIdx.x == 0 && kvh == 0 && tid == 0);
   const KeyRange kr = key_range(Tseq, p.q_len, qi, p.window, p.skip, p.split_target);
   const int T = kr.T, lo = kr.lo, C = kr.C;
-  if (T <= 0 || split >= kr.ns) return;
+  if (T <= 0 || split >= kr.ns) {
+    if (waits_for_prefix) grid_dependency_wait();
+    return;
+  }
   const int tok0 = kr.base + split * C;
   const int npages = (min(T, tok0 + C) - tok0 + kPage - 1) / kPage;
   const int nsplit_b = kr.ns;
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       if (j4 == 0) p.lse_part[pidx] = L > 0.f ? M + __log2f(L) : -INFINITY;
     }
   }
-  if (p.skip != 0) grid_dependency_wait();
+  if (waits_for_prefix) grid_dependency_wait();
   allow_dependent_launch();
 }
 

@@ -17,8 +17,10 @@ constexpr int kSplitTokens = MEMRA_SPLIT_TOKENS;            // smallest split
 constexpr int kSplitTokensMax = MEMRA_SPLIT_TOKENS_MAX;      // largest split
 constexpr int kSplitPagesMax = kSplitTokensMax / kPage;
 // Smallest split of a cascade call's own keys (the part after the shared
-// prefix): short, so that the few own keys of many sequences spread over the GPU.
-constexpr int kCascadeSplitTokens = 256;
+// prefix): short, so that the few own keys of many sequences spread over the
+// GPU, yet few enough CTAs that they run on the SMs the prefix pass leaves
+// free, beside it.
+constexpr int kCascadeSplitTokens = 512;
 
 // Split size of a range of T tokens: enough splits to give one long sequence
 // `target` CTAs per KV head, never below `min_tokens` (1024; 256 for a cascade

@@ -131,8 +131,8 @@ def _cascade(memra, c, prefix, **kw):
 def test_cascade_workspace_and_host_validation(memra):
     # 16 sequences of 4,860 tokens over a 4,096-token prefix, 32 query heads
     for D, chunk in ((128, 64), (256, 64)):
-        # own keys (764 of them) split no finer than 256 tokens: 3 partials per row
-        rows, chunks, ns = 16 * 32, 4096 // chunk, 3
+        # own keys (764 of them) split no finer than 512 tokens: 2 partials per row
+        rows, chunks, ns = 16 * 32, 4096 // chunk, 2
         suf = ((rows * ns * D * 4 + 255) // 256) * 256 + rows * ns * 4
         pre_o = rows * chunks * D * 4
         want = ((suf + 255) // 256) * 256 + ((pre_o + 255) // 256) * 256 + rows * chunks * 4

@@ -194,7 +194,7 @@ def test_cascade_host_validation():
 
 @pytest.mark.parametrize("case", ["one_page_prefix", "ten_row_tiles", "d256_ragged"])
 def test_cascade_edges(case):
-    if case == "one_page_prefix":          # one chunk, no cluster partner
+    if case == "one_page_prefix":          # one chunk: one prefix CTA per KV head
         w = small(prefix=16, seq_lens=(17, 40, 300), seed=38)
     elif case == "ten_row_tiles":          # 40 sequences x q_len 4 x group 8 = 1,280 rows per KV head
         lens = [400 + 29 * i for i in range(40)]
@@ -218,7 +218,7 @@ def test_cascade_ctas_loop_over_chunks(D, n_kv_heads, prefix, q_len):
 
 def test_cascade_rescales_the_accumulator():
     # keys of one prefix chunk 8x larger: the row maxima jump by far more than the lazy margin.  With
-    # 640 chunks over 304 CTA slots a CTA takes 3 chunks, so chunk 301 (tokens 19,264 .. 19,327; prefix
+    # 640 chunks over 152 CTA slots a CTA takes 5 chunks, so chunk 301 (tokens 19,264 .. 19,327; prefix
     # rows are stored in token order) is the second of its CTA, which rescales O in tensor memory
     w = small(n_heads=8, n_kv_heads=1, prefix=40960, seq_lens=(41000, 41600), seed=42)
     k = w.k_rows.astype(np.float32)
