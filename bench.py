@@ -370,7 +370,10 @@ def main():
             memra.decode_step(dw.cache, k_new, v_new, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out,
                               dw.workspace, w.sm_scale, stream=stream)
 
-    launches_per_step = (3 if args.two_call else 2) + (1 if args.cascade else 0)
+    # the split kernel, the combine (left out when every row fits one split), the separate append of the
+    # two-call form, the cascade's prefix pass
+    combine = 1 if (args.cascade or w.max_seq_len > memra.SPLIT_TOKENS) else 0
+    launches_per_step = 1 + combine + (1 if args.two_call else 0) + (1 if args.cascade else 0)
 
     def step(ev0, ev1):
         # one pass of the hot path through the public entry points, events only

@@ -389,6 +389,9 @@ int decode_both_passes(const DecodeArgs &a, const void *k_new, const void *v_new
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = run_partials(a, k_new, v_new, s);
   if (st) return st;
+  // Every row fits one split (no split is shorter than kSplitTokens): the
+  // split pass wrote every row, zeros included, and there is nothing to merge.
+  if (a.max_seq_len > 0 && a.max_seq_len <= kSplitTokens) return MEMRA_OK;
   return run_combine(a.cache, a.seq_lens, a.max_seq_len, a.max_pages_per_seq, a.batch, a.q_len, a.n_heads,
                      a.head_dim, a.window, a.workspace, a.out, s);
 }

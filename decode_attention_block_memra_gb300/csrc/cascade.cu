@@ -1152,11 +1152,13 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
   __shared__ float red[W][D];
   __shared__ float redl[W];
   __shared__ float mx[W];
-  grid_dependency_wait();          // both passes are complete
   const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = row / (p.q_len * p.n_heads), qi = (row / p.n_heads) % p.q_len;
+  // the row's own-key plan before the wait: the lengths were complete before
+  // the call's first pass started
   const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, false, p.status, false);
   const int ns = min(key_range(Tseq, p.q_len, qi, 0, p.prefix_len, p.split_target).ns, p.nsplit_max);
+  grid_dependency_wait();          // both passes are complete
   const int parts = p.n_parts + ns;
   auto lse_of = [&](int k) {
     return k < p.n_parts ? p.lse_pre[static_cast<size_t>(row) * p.n_parts + k]
@@ -1180,8 +1182,8 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    // warp w takes parts w, w + W, ...: four of them in flight at a time
-    constexpr int BATCH = 4;
+    // warp w takes parts w, w + W, ...: eight of them in flight at a time
+    constexpr int BATCH = 8;
     for (int k0 = warp; k0 < parts; k0 += BATCH * W) {
       float ls[BATCH];
       float4 x[BATCH][PER / 4];

@@ -24,15 +24,18 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const Co
   __shared__ float red[kCombineMaxWarps][D];
   __shared__ float redl[kCombineMaxWarps];
   __shared__ float mx[kCombineMaxWarps];
-  grid_dependency_wait();                           // the split kernel's partials are complete
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int b = row / (p.q_len * p.n_heads);
   const int qi = (row / p.n_heads) % p.q_len;
-  // keys visible to this row's position (its own split plan, as in the split kernel)
+  // Keys visible to this row's position (its own split plan, as in the split
+  // kernel).  The lengths are read before the wait for the split kernel: they
+  // were complete before that kernel started, and this grid launches only once
+  // each of its CTAs has passed its own wait.
   const int Tseq = clamp_seq_len(p.seq_lens[b], p.q_len, p.max_seq_len, p.max_pages, p.ring, p.status, false);
   const int ns = key_range(Tseq, p.q_len, qi, p.window, 0, p.split_target).ns;
+  grid_dependency_wait();                           // the split kernel's partials are complete
   __half *dst = p.out + static_cast<size_t>(row) * D;
   if (ns == 0) {                                    // no visible key: zeros
     for (int j = threadIdx.x; j < D; j += blockDim.x) dst[j] = __float2half(0.f);

@@ -215,6 +215,16 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   const KeyRange kr = key_range(Tseq, p.q_len, qi, p.window, p.skip, p.split_target);
   const int T = kr.T, lo = kr.lo, C = kr.C;
   if (T <= 0 || split >= kr.ns) {
+    // A row with no visible key is zeros; split 0's CTA writes them, so that a
+    // call whose rows all fit one split needs no combine launch.
+    if (T <= 0 && split == 0 && p.skip == 0) {
+      const int nr = min(8, p.group - 8 * hg);
+      for (int i = tid; i < nr * (D / 8); i += kWarpsFor<D> * 32) {
+        const int head = kvh * p.group + 8 * hg + i / (D / 8);
+        const size_t rowid = (static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head;
+        *reinterpret_cast<uint4 *>(p.out + rowid * D + 8 * (i % (D / 8))) = make_uint4(0, 0, 0, 0);
+      }
+    }
     if (waits_for_prefix) grid_dependency_wait();
     return;
   }

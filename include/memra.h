@@ -203,8 +203,10 @@ int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t 
 
 /* The two passes of memra_decode_attn, separately (same arguments and
  * meaning).  memra_decode_attn == partials followed by combine on one
- * stream.  Sequences that fit one split are written to `out` by the
- * partials pass directly; the combine pass merges the others. */
+ * stream (the combine is left out when max_seq_len <= 1024: every row then
+ * fits one split).  Rows that fit one split, and rows with no visible key
+ * (zeros), are written to `out` by the partials pass directly; the combine
+ * pass merges the others. */
 int memra_decode_attn_partials(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
                                int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
                                int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,

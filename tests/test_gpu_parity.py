@@ -173,6 +173,27 @@ def test_empty_batch_and_empty_sequence():
     assert torch.all(dw.out[1] == 0)
 
 
+def test_rows_without_keys_are_zeros_without_a_combine():
+    # contexts of at most 1,024 tokens fit one split, so the call launches no combine: a sequence
+    # shorter than q_len leaves its first rows without a visible key, and the split pass writes zeros
+    import decode_attention_block_memra_gb300 as memra
+    w = W.random_case(12, batch=2, q_len=4, n_heads=8, n_kv_heads=2, ctx=(300, 600))
+    assert w.max_seq_len <= memra.SPLIT_TOKENS
+    from decode_attention_block_memra_gb300.runner import upload
+    dw = upload(w)
+    dw.step()                                 # the step's rows are appended
+    assert memra.read_status(dw.cache) == 0
+    ref = attention.reference(w)
+    dw.seq_lens[0] = 2                        # rows 0 and 1 sit before position 0
+    dw.out.fill_(7)
+    memra.decode_attn(dw.cache, dw.q, dw.page_table, dw.seq_lens, w.max_seq_len, dw.out, dw.workspace, w.sm_scale)
+    assert memra.read_status(dw.cache) == memra.DEVERR_BAD_SEQ_LEN
+    out = dw.out.cpu().numpy().astype(np.float64)
+    assert (out[0, :2] == 0).all()
+    assert np.isfinite(out[0, 2:]).all() and not (out[0, 2:] == 7).any()
+    assert np.abs(out[1] - ref[1]).max() <= TOL
+
+
 def test_bad_page_and_slot_are_flagged_not_faulted():
     import decode_attention_block_memra_gb300 as memra
     w = W.random_case(11, batch=2, q_len=1, n_heads=8, n_kv_heads=2, ctx=(300, 900))
