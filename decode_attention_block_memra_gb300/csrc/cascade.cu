@@ -195,31 +195,34 @@ __device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, int
       // bytes 2 s + f of the word: (s = 0: f = 0, 1), (s = 1: f = 0, 1)
       e4m3x4_to_half2x2(r.lw[c], hi[0][c], hi[1][c]);
     } else {
-      float dh[2], mh[2];
-#pragma unroll
-      for (int f = 0; f < 2; ++f) {
-        dh[f] = 0.5f * __half2float(__ushort_as_half(static_cast<unsigned short>(r.dw[c] >> (16 * f))));
-        mh[f] = 0.5f * __half2float(__ushort_as_half(static_cast<unsigned short>(r.mw[c] >> (16 * f))));
-      }
+      // Both tokens of the pair (f = 0, 1) at once: their codes sit 16 bits
+      // apart in the words, and their scales are the two halves of dw, mw.
+      // The value, halved, is d q/2 (+ m/2 for q5_1) as hi + lo fp16 parts:
+      // the product rounded and its exact residual (one FMA), and for q5_1
+      // the rounded sum with m/2 and its exact error (TwoSum).  The _rn
+      // operations are never contracted into FMAs, which keeps both exact.
+      const __half2 d2 = bits_h2(r.dw[c]);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
-        float x[2];
-#pragma unroll
-        for (int f = 0; f < 2; ++f) {
-          const int k = 2 * f + ph;
-          uint32_t q = (r.lw[c] >> (8 * k + 4 * s)) & 15u;
-          // the code as an exact float: 2^23 + q, less 2^23 (q5_1) or 2^23 + 8 (q4_0)
-          if constexpr (VF == MEMRA_KV_Q5_1) {
-            q |= ((r.hw[c] >> (8 * k + 4 * s + 2 * (b & 1) + h)) & 1u) << 4;
-            x[f] = fmaf(dh[f], __uint_as_float(0x4B000000u | q) - 8388608.f, mh[f]);
-          } else {
-            x[f] = dh[f] * (__uint_as_float(0x4B000000u | q) - 8388616.f);
-          }
+        const int sh = 8 * ph + 4 * s;
+        uint32_t codes = (r.lw[c] >> sh) & 0x000F000Fu;
+        if constexpr (VF == MEMRA_KV_Q5_1) codes |= ((r.hw[c] >> (sh + 2 * (b & 1) + h)) & 0x00010001u) << 4;
+        // 1024 + q as fp16, then q/2 (q5_1) or (q - 8)/2 (q4_0), exactly
+        const __half2 q2 = __hfma2(bits_h2(codes | 0x64006400u), __float2half2_rn(0.5f),
+                                   __float2half2_rn(VF == MEMRA_KV_Q5_1 ? -512.f : -516.f));
+        const __half2 p_hi = __hmul2_rn(q2, d2);
+        const __half2 p_lo = __hfma2(q2, d2, __hneg2(p_hi));
+        if constexpr (VF == MEMRA_KV_Q5_1) {
+          const __half2 m2 = __hmul2_rn(bits_h2(r.mw[c]), __float2half2_rn(0.5f));
+          const __half2 s2 = __hadd2_rn(p_hi, m2);
+          const __half2 bb = __hsub2_rn(s2, p_hi);
+          const __half2 e2 = __hadd2_rn(__hsub2_rn(p_hi, __hsub2_rn(s2, bb)), __hsub2_rn(m2, bb));
+          hi[s][c] = h2_bits(s2);
+          lo[s][c] = h2_bits(__hadd2_rn(e2, p_lo));
+        } else {
+          hi[s][c] = h2_bits(p_hi);
+          lo[s][c] = h2_bits(p_lo);
         }
-        const __half2 h2 = __floats2half2_rn(x[0], x[1]);
-        const float2 back = __half22float2(h2);
-        hi[s][c] = h2_bits(h2);
-        lo[s][c] = h2_bits(__floats2half2_rn(x[0] - back.x, x[1] - back.y));
       }
     }
   }
