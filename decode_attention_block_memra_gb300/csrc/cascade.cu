@@ -8,27 +8,32 @@
 // Here the query rows of one KV head -- every sequence, query position and
 // query head of its group, 128 to a tile -- are the M side of tcgen05 MMAs
 // whose accumulators live in tensor memory: the one place on the decode path
-// that is a dense contraction.  The attention is exact and comes in two parts
-// merged by log-sum-exp:
-//   * the prefix pass (cascade_prefix_kernel): CTA (chunk c, KV head h, row
-//     tile) stages the chunk's 128 prefix tokens (64 at head_dim 256) with bulk
-//     copies, dequantizes K and V once into fp16 tiles in shared memory,
-//     computes S = Q K^T (M = 128 rows, N = chunk tokens, K = head_dim) into
-//     tensor memory, the softmax of each row (one thread per row and column
-//     half), P in fp16 back to shared memory, O = P V (N = head_dim, K = chunk
-//     tokens) into tensor memory, and leaves (o = O / l, lse = m + log2 l);
-//   * the split kernel over each sequence's own keys, from the prefix end on;
+// that is a dense contraction.  The attention is exact and comes in three
+// launches merged by log-sum-exp:
+//   * the prefix pass: CTA (run of 64-token chunks, KV head, row tile) stages
+//     each chunk's prefix pages with bulk copies, dequantizes K and V once into
+//     fp16 tiles in shared memory, computes S = Q K^T (M = 128 rows, N = chunk
+//     tokens, K = head_dim) into tensor memory, keeps an online softmax per row
+//     across its chunks, writes P in fp16 back to shared memory and
+//     accumulates O += P V (N = head_dim, K = chunk tokens) in tensor memory.
+//     At the end it writes one partial per row, (o = O / l, lse = m + log2 l),
+//     the row by one bulk copy.  At head_dim 128 the pass is warp-specialized
+//     (cascade_prefix_ws_kernel: staging, MMA and softmax warps, one thread
+//     per row); at 256 its warps take the phases in turn (cascade_prefix_kernel,
+//     two threads per row, one per column half);
+//   * the split kernel over each sequence's own keys, from the prefix end on,
+//     on the SMs the prefix pass leaves free;
 //   * cascade_combine_kernel: the log-sum-exp merge of both, one CTA per row.
 //
-// Values enter the MMAs exactly: fp8 and NVFP4 codes (times their e4m3 block
-// scale) are exact in fp16, with the float32 tensor scale applied to the fp32
-// scores or output; a q8_0 / q5_1 / q4_0 value is staged at half its size as
-// an fp16 pair hi + lo (hi = fp16(x / 2), lo = fp16(x / 2 - hi), exact for
-// q8_0 and q4_0, within 2^-22 relative for q5_1's d q + m), both pairs enter
-// the same accumulator, and the factor 2 returns in fp32.  Halving keeps every
-// value of an fp16-range block finite.  A row's bytes depend on its own query
-// and the keys only (no value of one row enters another's), and on the prefix
-// length, which fixes the chunks.
+// Values enter the MMAs exactly, or nearly: fp8 and NVFP4 codes (times their
+// e4m3 block scale) are exact in fp16, with the float32 tensor scale applied to
+// the fp32 scores or output; a q8_0 / q5_1 / q4_0 value is staged at half its
+// size as an fp16 pair hi + lo (the rounded product and its exact residual:
+// exact for q8_0 and q4_0; q5_1's d q + m within ~2^-22 of the block's scale,
+// through a TwoSum with m), both parts enter the same accumulator, and the
+// factor 2 returns in fp32.  Halving keeps every value of an fp16-range block
+// finite.  A row's bytes depend on its own query and the keys only (no value of
+// one row enters another's), and on the prefix length, which fixes the chunks.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
