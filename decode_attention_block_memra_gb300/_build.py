@@ -2,9 +2,15 @@
 
 Each translation unit compiles in its own nvcc process, in parallel; the
 shared library links the CUDA runtime statically, so it needs only the driver.
+
+Staleness is decided by content, not by file times: a SHA-256 over the
+sources, the headers, the public header, this file and the compiler flags is
+written beside the library (libmemra.so.sha256), and the library is rebuilt
+whenever the stamp is missing or differs.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -15,6 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libmemra.so")
+STAMP = LIB + ".sha256"
 
 SOURCES = ["api.cu", "kv_append.cu", "combine.cu", "decode_d128.cu", "decode_d256.cu", "noalloc.cu", "cascade.cu"]
 HEADERS = ["memra_device.cuh", "decode_kernel.cuh", "kv_quant.cuh", "cascade.cuh", "tcgen05.cuh"]
@@ -30,14 +37,31 @@ def nvcc() -> str:
     return path
 
 
-def _newest_input() -> float:
+def source_hash() -> str:
+    """SHA-256 (first 16 hex digits) of everything the library is built from."""
+    h = hashlib.sha256()
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "memra.h"), __file__]
-    return max(os.path.getmtime(f) for f in files)
+    for f in files:
+        h.update(os.path.basename(f).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS[:-1]).encode())
+    return h.hexdigest()[:16]
+
+
+def built_hash() -> str | None:
+    """The source hash the present libmemra.so was built from (None if unstamped)."""
+    try:
+        with open(STAMP) as f:
+            return f.read().strip() or None
+    except FileNotFoundError:
+        return None
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libmemra.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    """Compile (unless the library's stamp matches the sources) and return the path of libmemra.so."""
+    want = source_hash()
+    if not force and os.path.exists(LIB) and built_hash() == want:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -61,6 +85,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP + ".tmp", "w") as f:
+        f.write(want + "\n")
+    os.replace(STAMP + ".tmp", STAMP)
     return LIB
 
 

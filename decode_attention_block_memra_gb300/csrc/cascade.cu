@@ -28,10 +28,14 @@
 // Values enter the MMAs exactly, or nearly: fp8 and NVFP4 codes (times their
 // e4m3 block scale) are exact in fp16, with the float32 tensor scale applied to
 // the fp32 scores or output; a q8_0 / q5_1 / q4_0 value is staged at half its
-// size as an fp16 pair hi + lo (the rounded product and its exact residual:
-// exact for q8_0 and q4_0; q5_1's d q + m within ~2^-22 of the block's scale,
-// through a TwoSum with m), both parts enter the same accumulator, and the
-// factor 2 returns in fp32.  Halving keeps every value of an fp16-range block
+// size as an fp16 pair hi + lo (the rounded product and its residual from one
+// FMA; for q5_1 also a TwoSum with m/2), both parts enter the same accumulator,
+// and the factor 2 returns in fp32.  The pair is exact for q8_0 and q4_0 while
+// the residual is representable: its last bit is ulp(d)/2 (halved value), so
+// exact for d >= 2^-13; for smaller d the residual is rounded to an fp16
+// subnormal, off by at most 2^-25 (2^-24 on the value).  q5_1's d q + m is
+// within ~2^-22 of the block's scale, and also within 2^-24 absolute when m/2
+// or the residual falls below the fp16 subnormal step.  Halving keeps every value of an fp16-range block
 // finite.  A row's bytes depend on its own query and the keys only (no value of
 // one row enters another's), and on the prefix length, which fixes the chunks.
 #include <cuda_fp16.h>
@@ -203,9 +207,11 @@ __device__ __forceinline__ void convert_v_task(const VRaw &r, int ph, int b, int
       // Both tokens of the pair (f = 0, 1) at once: their codes sit 16 bits
       // apart in the words, and their scales are the two halves of dw, mw.
       // The value, halved, is d q/2 (+ m/2 for q5_1) as hi + lo fp16 parts:
-      // the product rounded and its exact residual (one FMA), and for q5_1
-      // the rounded sum with m/2 and its exact error (TwoSum).  The _rn
-      // operations are never contracted into FMAs, which keeps both exact.
+      // the product rounded and its residual (one FMA), and for q5_1 the
+      // rounded sum with m/2 and its error (TwoSum).  The _rn operations are
+      // never contracted into FMAs.  The parts are exact while the residual
+      // is representable in fp16 (d >= 2^-13); below that, the residual and
+      // m/2 are rounded to fp16 subnormals (at most 2^-25 off each).
       const __half2 d2 = bits_h2(r.dw[c]);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {

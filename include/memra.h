@@ -313,8 +313,10 @@ int memra_decode_step_cascade(const memra_kv_cache *cache, const void *k_new, co
  *   - Returns MEMRA_ERR_WORKSPACE when memra_decode_attn_workspace_bytes(batch,
  *     q_len, n_heads, head_dim, max_seq_len) exceeds MEMRA_NOALLOC_SCRATCH_BYTES.
  *   - The first call on a device looks up the array's device address (a CUDA
- *     runtime query, no allocation); make that first call before any stream
- *     capture.
+ *     runtime query, no allocation) and keeps it for later calls; make that
+ *     first call before any stream capture.  The kept address belongs to the
+ *     device's current context: after cudaDeviceReset it is stale, so do not
+ *     call this entry point again in a process that reset the device.
  *   - Every call shares the array and leaves its bytes behind; nothing in it
  *     needs to start at zero.  Calls whose kernels may overlap on the GPU
  *     (unordered streams) race on the array and must be serialized. */

@@ -148,3 +148,26 @@ def test_cascade_workspace_and_host_validation(memra):
     assert _cascade(memra, c, 48, wsb=10) == 3              # workspace too small
     assert _cascade(memra, c, 80, maxlen=100) == 1          # five prefix pages, four table columns
     assert _cascade(memra, c, 16, B=0) == 0                 # empty batch: no-op
+
+
+def _header_defines():
+    text = open(HEADER).read()
+    out = {}
+    for name, val in re.findall(r"^#define\s+(MEMRA_[A-Z0-9_]+)\s+(.+?)\s*(?:/\*.*)?$", text, flags=re.M):
+        out[name] = val
+    return out
+
+
+def test_binding_constants_match_the_header():
+    """The Python binding's copies of the header's constants agree with include/memra.h."""
+    import decode_attention_block_memra_gb300 as m
+    d = _header_defines()
+
+    def value(name):
+        return int(eval(d[name].replace("u", ""), {}))           # e.g. "(16u << 20)"
+
+    assert value("MEMRA_NOALLOC_SCRATCH_BYTES") == m.NOALLOC_SCRATCH_BYTES
+    assert value("MEMRA_PAGE_SIZE") == m.PAGE_SIZE
+    assert value("MEMRA_SPLIT_TOKENS") == m.SPLIT_TOKENS
+    for bit in ("BAD_PAGE", "BAD_SLOT", "BAD_SEQ_LEN", "TIMEOUT", "PREFIX"):
+        assert value("MEMRA_DEVERR_" + bit) == getattr(m, "DEVERR_" + bit)

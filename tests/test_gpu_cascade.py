@@ -234,3 +234,19 @@ def test_cascade_full_size_long_shared_prefix():
     res = run(w, fused=True)
     assert res.flags == 0
     assert_close(w, res.out, attention.reference(w))
+
+
+@pytest.mark.parametrize("kf,vf", [("q8_0", "q5_1"), ("q8_0", "q4_0")])
+def test_cascade_tiny_block_scales(kf, vf):
+    # K and V scaled by 1e-3: block scales near 2^-16, below 2^-13, where the staged hi + lo fp16 pair
+    # loses the residual's last bits to fp16 subnormals (at most 2^-24 off a value).  The scores are
+    # scaled up again through q so the softmax is not uniform
+    w = small(kf, vf, prefix=1024, seq_lens=(1100, 1500, 1030), seed=43)
+    w.k_rows = (w.k_rows.astype(np.float32) * 1e-3).astype(np.float16)
+    w.v_rows = (w.v_rows.astype(np.float32) * 1e-3).astype(np.float16)
+    w.q = np.clip(w.q.astype(np.float32) * 1e3, -60000, 60000).astype(np.float16)
+    ref = attention.reference(w)
+    res = run(w)
+    assert res.flags == 0
+    # the outputs are ~1e-3 in size: hold them to 2e-3 relative to that scale (x 8 for the largest values)
+    assert_close(w, res.out, ref, tol=2e-3 * 1e-3 * 8)

@@ -1,9 +1,11 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
 
 Quantized blocks must match the oracle bit for bit; attention outputs within
-max |gpu - oracle| <= 2e-3 (fp16 output of fp32-accumulated attention, see
-the tolerance derivation in the design doc).  The pools start as seeded random
-bytes, so slots that were never written hold garbage the kernels must ignore.
+max |gpu - oracle| <= 2e-3.  That bound covers the fp16 rounding of the output
+(2^-11 |o|, below 1e-3 for |o| < 2) plus the fp16 rounding of the softmax
+weights before the P.V product and float32 accumulation; the K and V codes
+enter the products exactly.  The pools start as seeded random bytes, so slots
+that were never written hold garbage the kernels must ignore.
 """
 from types import SimpleNamespace
 

@@ -17,8 +17,6 @@ import workloads as W
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-TOL = 2e-3
-
 
 @pytest.fixture(scope="module")
 def memra():
@@ -53,10 +51,10 @@ def test_noalloc_matches_workspace_entry_point(memra, case):
     else:
         w = W.random_case(62, batch=2, q_len=4, n_heads=32, n_kv_heads=4, head_dim=128, ctx=(2000, 3500))
     want, got = _outputs(memra, w)
+    # the same kernels on the same inputs: the bytes must match the workspace call's exactly
     for g in got:
         assert torch.isfinite(g.float()).all()
-        err = (g.float() - want.float()).abs().max().item()
-        assert err <= TOL, err
+        assert torch.equal(g.view(torch.int16), want.view(torch.int16))
 
 
 def test_noalloc_rejects_sizes_beyond_the_array(memra):
