@@ -12,6 +12,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import full_parity
 import workloads as W
 from oracle import attention
 
@@ -92,11 +93,13 @@ def test_cascade_group_and_heads(D):
     assert_close(w, res.out, attention.reference(w))
 
 
-def test_cascade_full_size_shared_prefix():
+@pytest.mark.parametrize("fused", [False, True])
+def test_cascade_full_size_shared_prefix(fused):
+    # every output row and (fused: the step's rows stored by the cascade call) every pool byte
     w = W.shared_prefix()
-    res = run(w)
+    res = run(w, fused=fused, want_pools=True)
     assert res.flags == 0
-    assert_close(w, res.out, attention.reference(w))
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
 
 
 def _device_case(w):
@@ -231,9 +234,9 @@ def test_cascade_rescales_the_accumulator():
 
 def test_cascade_full_size_long_shared_prefix():
     w = W.shared_prefix_long()
-    res = run(w, fused=True)
+    res = run(w, fused=True, want_pools=True)
     assert res.flags == 0
-    assert_close(w, res.out, attention.reference(w))
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
 
 
 @pytest.mark.parametrize("kf,vf", [("q8_0", "q5_1"), ("q8_0", "q4_0")])

@@ -12,6 +12,7 @@ from types import SimpleNamespace
 import numpy as np
 import pytest
 
+import full_parity
 import workloads as W
 from oracle import attention, layout, quant
 
@@ -42,19 +43,6 @@ def assert_pools_exact(w, res, cache=None):
         if not np.array_equal(want, got):
             bad = np.argwhere(want != got)
             raise AssertionError(f"{name} pool differs at {len(bad)} bytes, first (page, head, byte) {bad[:5].tolist()}")
-
-
-def assert_rows_exact(w, res, rows, cache):
-    """Decode sampled rows from the GPU pools and compare their fields with the oracle's."""
-    for h in range(w.n_kv_heads):
-        for side, fmt, pool, scale in (("k", w.k_fmt, res.k_pool, w.k_scale), ("v", w.v_fmt, res.v_pool, w.v_scale)):
-            got = layout.read_rows(pool, side, fmt, w.slots[rows], h, w.head_dim, scale)
-            want = quant.select_rows(cache[side][h], rows)
-            for key in ("q", "d", "m", "sb"):
-                if key in want:
-                    a = np.asarray(got[key]).view(np.uint8)
-                    b = np.asarray(want[key]).view(np.uint8)
-                    assert np.array_equal(a, b), f"{side} {fmt} field {key} differs (head {h})"
 
 
 def assert_out_close(w, res, ref, tol=TOL):
@@ -254,29 +242,21 @@ def test_batch_invariance_and_determinism():
 
 
 # ------------------------------------------------------ full-size workloads --
+# Every output row and every pool byte of the five workloads at their full
+# sizes, against the oracle spread over the host's cores (tests/full_parity.py).
 
-def _sample_rows(w, n, seed):
-    rng = np.random.default_rng(seed)
-    B, Q, Hq, _ = w.q.shape
-    picks = {(int(rng.integers(B)), int(rng.integers(Q)), int(rng.integers(Hq))) for _ in range(n)}
-    picks.add((B - 1, Q - 1, Hq - 1))
-    return sorted(picks)
+def check_everything(w, res):
+    s = full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
+    assert s["rows"] == w.batch * w.q_len * w.n_heads
+    return s
 
 
-@pytest.mark.parametrize("name", ["shared_prefix", "long_context", "mtp_verify"])
+@pytest.mark.parametrize("name", ["tiny", "shared_prefix", "long_context", "mtp_verify"])
 def test_full_size_workloads(name):
     w = W.WORKLOADS[name]()
-    cache = attention.quantize_cache(w)
     res = run(w)
     assert res.flags == 0
-    if name == "long_context":
-        rows = np.random.default_rng(0).choice(w.slots.size, 20000, replace=False)
-        rows = np.union1d(rows, w.step_rows)
-        assert_rows_exact(w, res, rows, cache)
-        assert_out_close(w, res, attention.reference(w, cache=cache))
-    else:
-        assert_pools_exact(w, res, cache=cache)
-        assert_out_close(w, res, attention.reference(w, cache=cache, rows=_sample_rows(w, 48, 1)))
+    check_everything(w, res)
 
 
 @pytest.fixture(scope="module")
@@ -290,27 +270,7 @@ def test_format_sweep_full_size(sweep_base, variant):
     w = sweep_base.with_formats(kf, vf)
     res = run(w)
     assert res.flags == 0
-    rows = np.random.default_rng(1).choice(w.slots.size, 4000, replace=False)
-    rows = np.union1d(rows, w.step_rows)
-    picks = _sample_rows(w, 24, 2)
-    seqs = sorted({b for b, _, _ in picks})
-    # oracle quantization of just the rows it needs
-    need = np.union1d(rows, np.concatenate([attention.sequence_rows(w, b) for b in seqs]))
-    cache = {"k": [], "v": []}
-    for h in range(w.n_kv_heads):
-        for side, fmt, src, sc in (("k", kf, w.k_rows, w.k_scale), ("v", vf, w.v_rows, w.v_scale)):
-            sub = quant.quantize_rows(src[need, h, :], fmt, sc)
-            full = {"fmt": fmt}
-            for key, val in sub.items():
-                if isinstance(val, np.ndarray):
-                    arr = np.zeros((w.slots.size,) + val.shape[1:], dtype=val.dtype)
-                    arr[need] = val
-                    full[key] = arr
-                elif key != "fmt":
-                    full[key] = val
-            cache[side].append(full)
-    assert_rows_exact(w, res, rows, cache)
-    assert_out_close(w, res, attention.reference(w, cache=cache, rows=picks))
+    check_everything(w, res)
 
 
 def _adversarial_rows(rng, n, D):
@@ -438,14 +398,12 @@ def test_fused_step_adversarial_rows(kf, vf):
     assert np.isfinite(res.out.astype(np.float32)).all()
 
 
-def test_fused_step_full_size_long_context():
-    w = W.WORKLOADS["long_context"]()
-    cache = attention.quantize_cache(w)
+@pytest.mark.parametrize("name", ["long_context", "mtp_verify"])
+def test_fused_step_full_size(name):
+    w = W.WORKLOADS[name]()
     res = run_fused(w)
     assert res.flags == 0
-    rows = np.union1d(np.random.default_rng(3).choice(w.slots.size, 5000, replace=False), w.step_rows)
-    assert_rows_exact(w, res, rows, cache)
-    assert_out_close(w, res, attention.reference(w, cache=cache))
+    check_everything(w, res)
 
 
 def test_fused_step_bad_page_and_validation():
@@ -519,7 +477,7 @@ def test_verify_rows_equal_plain_decode(K):
     w = W.make_workload(f"verify_k{K}", batch=4, q_len=Q, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
                         v_fmt="q5_1", seed=40 + K, seq_lens=seq_lens, permute_pages=True, extra_pages=2)
     out = _verify_vs_decode(w, fused=(K % 2 == 0))
-    ref = attention.reference(w, rows=_sample_rows(w, 24, K))
+    ref = attention.reference(w)
     assert_out_close(w, SimpleNamespace(out=out), ref)
 
 
@@ -647,12 +605,9 @@ def test_nvfp4_fused_step_and_adversarial_blocks():
 
 def test_nvfp4_full_size_long_context():
     w = W.WORKLOADS["long_context"]().with_formats("nvfp4", "nvfp4")
-    cache = attention.quantize_cache(w)
     res = run(w)
     assert res.flags == 0
-    rows = np.union1d(np.random.default_rng(4).choice(w.slots.size, 5000, replace=False), w.step_rows)
-    assert_rows_exact(w, res, rows, cache)
-    assert_out_close(w, res, attention.reference(w, cache=cache))
+    check_everything(w, res)
 
 
 # -------------------------------------------- numeric class across formats --
