@@ -305,21 +305,45 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   // product [16 tokens x blocks] x [blocks x rows]: one more MMA per page with
   // A = the page's block scales and B = -1152 sumQ_b split into fp16 hi + lo
   // parts (k slots 0..nb-1 hi, nb..2nb-1 lo), exact to ~2^-22.
+  // 1152 sumQ_b must stay inside fp16's range: a row whose block sums pass 32
+  // in magnitude enters the MMAs as Q 2^-e (e >= 1, the fewest that bring them
+  // to 32 or below), and its fp32 score scale takes the 2^e back.  e depends
+  // on the row's own query only; ordinary queries (|sum| <= 32) keep e = 0.
   uint32_t corrb[NT][2];
+  float row_scale[NT][2] = {};     // fp32 score scale of rows 8n + 2c, 8n + 2c + 1
   if constexpr (kK8) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      float csum[NB];
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) {
+      auto block_sum = [&](int bb) {
         const __half2 *h = reinterpret_cast<const __half2 *>(&qf[n][bb]);
         float2 a = __half22float2(h[0]), b2 = __half22float2(h[1]), c2 = __half22float2(h[2]),
                d2 = __half22float2(h[3]);
         float sum = ((a.x + a.y) + (b2.x + b2.y)) + ((c2.x + c2.y) + (d2.x + d2.y));
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);          // row 8n+g, whole block
-        csum[bb] = -1152.f * sum;
+        return sum;
+      };
+      float amax = 0.f;
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) amax = fmaxf(amax, fabsf(block_sum(bb)));
+      int qe = 0;                                   // |sum| <= 32 * 65504 < 2^21: qe <= 16
+      while (qe < 16 && amax > ldexpf(32.f, qe)) ++qe;
+      if (qe > 0) {
+        const uint32_t down = pack_half2(ldexpf(1.f, -qe), ldexpf(1.f, -qe));   // exact power of two
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          qf[n][bb].x = hmul2_u32(qf[n][bb].x, down);
+          qf[n][bb].y = hmul2_u32(qf[n][bb].y, down);
+          qf[n][bb].z = hmul2_u32(qf[n][bb].z, down);
+          qf[n][bb].w = hmul2_u32(qf[n][bb].w, down);
+        }
       }
+      // rows 2c and 2c + 1 of the score fragments are held by the lanes of g = 2c, 2c + 1
+      row_scale[n][0] = ldexpf(p.scale_log2, __shfl_sync(0xffffffffu, qe, 8 * c));
+      row_scale[n][1] = ldexpf(p.scale_log2, __shfl_sync(0xffffffffu, qe, 8 * c + 4));
+      float csum[NB];
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) csum[bb] = -1152.f * block_sum(bb);
       // B[k][row g]: thread (g, c) holds k = 2c, 2c+1 (b0b1) and 2c+8, 2c+9 (b2b3)
       uint32_t bw[2];
 #pragma unroll
@@ -542,8 +566,15 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
         float mx[NT][2];
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
+          if constexpr (kK8) {
+            s4[n][0] = sc[n][0] * row_scale[n][0];
+            s4[n][1] = sc[n][1] * row_scale[n][1];
+            s4[n][2] = sc[n][2] * row_scale[n][0];
+            s4[n][3] = sc[n][3] * row_scale[n][1];
+          } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) s4[n][e] = sc[n][e] * p.scale_log2;
+          }
           if (masked) {
             const int t0 = pos0 + g, t1 = pos0 + g + 8;
             const bool v0 = t0 < T && t0 >= lo, v1 = t1 < T && t1 >= lo;

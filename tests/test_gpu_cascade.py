@@ -253,3 +253,13 @@ def test_cascade_tiny_block_scales(kf, vf):
     assert res.flags == 0
     # the outputs are ~1e-3 in size: hold them to 2e-3 relative to that scale (x 8 for the largest values)
     assert_close(w, res.out, ref, tol=2e-3 * 1e-3 * 8)
+
+
+def test_cascade_large_queries():
+    # the own-key split pass shares the plain kernel's q8_0 bias correction: large queries there too
+    w = small(prefix=1024, seq_lens=(1100, 1500, 1030), seed=44)
+    w.q = np.clip(w.q.astype(np.float32) * 1e3, -60000, 60000).astype(np.float16)
+    w.k_rows = (w.k_rows.astype(np.float32) * 1e-3).astype(np.float16)
+    res = run(w)
+    assert res.flags == 0
+    assert_close(w, res.out, attention.reference(w))

@@ -698,3 +698,43 @@ def test_append_every_fp16_value_bit_exact(fmt, side):
     exp = want.reshape(-1)[written]
     bad = np.nonzero(got != exp)[0]
     assert bad.size == 0, f"{bad.size} bytes differ"
+
+
+# --------------------------------------------------- large query magnitudes --
+# q8_0 keys enter the MMAs as biased codes, and the bias correction carries
+# 1152 * (sum of a 32-element block of q) in fp16: a query whose block sums pass
+# ~57 must still give the right scores (the row is scaled by a power of two).
+
+def _large_query_case(seed, kf, vf, D, q_len=1, heads_scaled=None):
+    w = W.random_case(seed, batch=3, q_len=q_len, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt=kf, v_fmt=vf,
+                      ctx=(q_len + 40, 2600))
+    q = w.q.astype(np.float32)
+    sel = slice(None) if heads_scaled is None else heads_scaled
+    q[:, :, sel, :] *= 1e3                          # |q| up to ~4,500; block sums up to ~30,000
+    w.q = q.astype(np.float16)
+    w.k_rows = (w.k_rows.astype(np.float32) * 1e-3).astype(np.float16)
+    w.k_scale, w.v_scale = W._fp8_scales(w)
+    return w
+
+
+@pytest.mark.parametrize("kf,vf,D", [("q8_0", "q5_1", 128), ("q8_0", "q4_0", 256), ("fp8", "q5_1", 128),
+                                     ("nvfp4", "q4_0", 128)])
+def test_large_query_magnitudes(kf, vf, D):
+    w = _large_query_case(600 + D, kf, vf, D)
+    res = run(w)
+    assert res.flags == 0
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_large_and_ordinary_query_rows_in_one_cta():
+    # heads 2, 3, 9 scaled up, the others ordinary: each row of an 8-head CTA keeps its own scale
+    w = _large_query_case(611, "q8_0", "q5_1", 128, heads_scaled=[2, 3, 9])
+    res = run(w)
+    assert res.flags == 0
+    assert_out_close(w, res, attention.reference(w))
+
+
+def test_large_query_verify_rows_equal_plain_decode():
+    w = _large_query_case(612, "q8_0", "q5_1", 128, q_len=4, heads_scaled=[0, 5, 6, 7, 12])
+    out = _verify_vs_decode(w, fused=True)
+    assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
