@@ -94,6 +94,11 @@ _SIGS = {
     "memra_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p, ctypes.c_void_p,
                                                  ctypes.c_int32, ctypes.c_void_p] + [ctypes.c_int32] * 6 +
                                   [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
+    "memra_testing_decode_attn_short_page": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.c_void_p,
+                                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p] +
+                                             [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_void_p,
+                                                                     ctypes.c_size_t, ctypes.c_void_p,
+                                                                     ctypes.c_uint64, ctypes.c_void_p]),
     "memra_read_status": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.POINTER(ctypes.c_int32),
                                          ctypes.c_void_p]),
     "memra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -290,6 +295,15 @@ def decode_attn_noalloc(cache: KVCache, q, page_table, seq_lens, max_seq_len: in
                                            _ptr(seq_lens), int(max_seq_len), B, Q, Hq, cache.n_kv_heads, D,
                                            float(sm_scale if sm_scale is not None else D ** -0.5), _ptr(out),
                                            _stream(stream)), "memra_decode_attn_noalloc")
+
+
+def testing_decode_attn_short_page(cache: KVCache, q, page_table, seq_lens, max_seq_len: int, out, workspace,
+                                   page_wait_ns: int, sm_scale=None, stream=None) -> None:
+    """memra_testing_decode_attn_short_page (memra_testing.h): decode attention whose first CTA's first
+    page wait cannot complete and runs out after page_wait_ns; the call then flags DEVERR_TIMEOUT."""
+    a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
+    _check(lib().memra_testing_decode_attn_short_page(*a, int(page_wait_ns), _stream(stream)),
+           "memra_testing_decode_attn_short_page")
 
 
 def read_status(cache: KVCache, stream=None) -> int:

@@ -40,7 +40,8 @@ def nvcc() -> str:
 def source_hash() -> str:
     """SHA-256 (first 16 hex digits) of everything the library is built from."""
     h = hashlib.sha256()
-    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "memra.h"), __file__]
+    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [__file__]
+    files += [os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h")]
     for f in files:
         h.update(os.path.basename(f).encode() + b"\0")
         with open(f, "rb") as fh:

@@ -9,6 +9,7 @@
 
 #include "cascade.cuh"
 #include "decode_kernel.cuh"
+#include "memra_testing.h"
 
 using namespace memra;
 
@@ -134,6 +135,9 @@ struct DecodeArgs {
   void *out;
   int32_t window;     // sliding window (tokens); > 0 also makes page_table rows rings
   int32_t prefix = 0; // cascade: tokens shared by every sequence, attended by the prefix pass
+  // test hooks of the bounded waits (memra_testing.h): 0 = the normal limit / no short page
+  uint64_t test_wait_ns = 0;
+  int32_t test_extra_tx = 0;
 };
 
 // Workspace of a cascade call: the split kernel's partials over each
@@ -271,6 +275,8 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   p.scale_log2 = a.sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = scaled_format(c.v_fmt) ? c.v_scale : 1.f;
   p.k_scale = c.k_scale;
+  p.page_wait_ns = a.test_wait_ns ? a.test_wait_ns : kWaitLimitNs;
+  p.test_extra_tx = a.test_extra_tx;
   // no position has more splits than min(ceil(L/min), max(target, ceil(L/8192))), L its key range
   const int64_t L = a.prefix > 0 ? range_max : longest_range(a.max_seq_len, a.window);
   const int64_t most = std::min<int64_t>(ceil_div(L, min_split),
@@ -572,3 +578,22 @@ int32_t memra_num_splits(int32_t seq_len) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ test hooks --
+// memra_testing.h: the decode call with a shortened page-wait limit and one
+// page whose wait cannot complete, to drive the bounded-wait path on a GPU.
+extern "C" int memra_testing_decode_attn_short_page(const memra_kv_cache *cache, const void *q,
+                                                    const int32_t *page_table, int32_t max_pages_per_seq,
+                                                    const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                                                    int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                                                    int32_t head_dim, float sm_scale, void *workspace,
+                                                    size_t workspace_bytes, void *out, uint64_t page_wait_ns,
+                                                    void *stream) {
+  if (page_wait_ns == 0 || page_wait_ns > kWaitLimitNs) return MEMRA_ERR_INVALID_ARG;
+  DecodeArgs a{cache, q, page_table, max_pages_per_seq, seq_lens, max_seq_len, batch, q_len, n_heads,
+               n_kv_heads, head_dim, sm_scale, workspace, workspace_bytes, out, 0};
+  a.test_wait_ns = page_wait_ns;
+  a.test_extra_tx = 16;
+  return decode_both_passes(a, nullptr, nullptr, stream);
+}
+

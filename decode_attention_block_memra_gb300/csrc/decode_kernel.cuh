@@ -78,6 +78,12 @@ struct DecodeParams {
   int ngh_q;          // CTAs per (split, KV head, sequence): q_len * ngh
   int nsplit_max, num_stages, split_target;
   float scale_log2, v_scale, k_scale;
+  // Test hooks of the bounded waits (memra_testing.h); kWaitLimitNs and 0 in
+  // every other call.  page_wait_ns bounds the waits for pages in the main
+  // loop; test_extra_tx > 0 makes CTA (0, 0, 0) expect that many bytes more
+  // than the copies of its first page deliver, so that page's wait runs out.
+  unsigned long long page_wait_ns;
+  int test_extra_tx;
 };
 
 struct CombineParams {
@@ -258,7 +264,9 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
     const int pid = pid_s[i];
     const uint32_t bar = full0 + 8 * s;
     if (pid >= 0) {
-      mbar_arrive_expect_tx(bar, STAGE);
+      const bool short_page = p.test_extra_tx > 0 && i == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+                              blockIdx.z == 0;
+      mbar_arrive_expect_tx(bar, STAGE + (short_page ? p.test_extra_tx : 0));
       bulk_copy_g2s(ring + s * STAGE, kbase + static_cast<size_t>(pid) * kstride, KSEG, bar, pol);
       bulk_copy_g2s(ring + s * STAGE + KSEG, vbase + static_cast<size_t>(pid) * vstride, VSEG, bar, pol);
     } else {
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   int s = r, par = 0;            // stage and phase parity of page i
   int stop_at = -1;              // page whose wait gave up, if any
   for (int i = r; i < npages; i += R) {
-    if (!mbar_wait_bounded(full0 + 8 * s, par, p.status)) {
+    if (!mbar_wait_bounded(full0 + 8 * s, par, p.status, p.page_wait_ns)) {
       stop_at = i;
       break;
     }
@@ -799,12 +807,14 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       par ^= 1;
     }
   }
-  // A wait that gave up: stay until this lane's copies in flight have landed
-  // (bounded), so no bulk copy outlives the CTA's shared memory.
+  // A wait that gave up: stay until this lane's copies in flight have landed,
+  // so no bulk copy outlives the CTA's shared memory.  Each of those waits has
+  // the full limit; a stage whose phase cannot complete (its expected bytes
+  // were never all sent) costs one limit and holds no copy in flight, since a
+  // copy's bytes land before they count against the phase.
   if (stop_at >= 0 && lane == 0) {
-    for (int j = stop_at; j < min(stop_at + NS, npages); j += R) {
-      if (!mbar_wait_bounded(full0 + 8 * (j % NS), (j / NS) & 1, p.status)) break;
-    }
+    for (int j = stop_at; j < min(stop_at + NS, npages); j += R)
+      mbar_wait_bounded(full0 + 8 * (j % NS), (j / NS) & 1, p.status);
   }
 
   // ------------------------------------------------------ merge the warps --

@@ -1,0 +1,46 @@
+/*
+ * memra_testing.h - test hook of the decode library (libmemra.so), not part
+ * of the decode ABI in memra.h.  The memra pages have no counterpart: it
+ * exists so that a test can drive, on a real GPU, the path that every
+ * pipeline wait of the split kernel takes when it runs out.
+ *
+ * Every wait of the library's kernels is bounded (about 1 s): past the bound
+ * the kernel ORs MEMRA_DEVERR_TIMEOUT into *cache->status, stays until the
+ * copies it issued itself have landed (each of those waits bounded too), and
+ * returns; it never traps and leaves no copy in flight.
+ */
+#ifndef MEMRA_TESTING_H
+#define MEMRA_TESTING_H
+
+#include <stdint.h>
+
+#include "memra.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* memra_decode_attn (same arguments, layout and ownership) with two changes
+ * inside its split kernel:
+ *   - the waits for pages in the main loop give up after page_wait_ns
+ *     nanoseconds (1 .. 1e9) instead of about 1 s;
+ *   - the CTA of the first split, first KV head and first sequence declares
+ *     16 bytes more than the copies of its first page deliver, so the wait
+ *     for that page cannot complete: it runs out, sets MEMRA_DEVERR_TIMEOUT
+ *     and that CTA's warp leaves its page loop.
+ * The waits for the copies still in flight keep the full limit, so the call
+ * takes about one second of GPU time.  The output is then invalid (the status
+ * says so); the pools, the workspace and any later call are unaffected.
+ * Returns MEMRA_ERR_INVALID_ARG for page_wait_ns outside 1 .. 1e9, otherwise
+ * what memra_decode_attn returns for these arguments. */
+int memra_testing_decode_attn_short_page(const memra_kv_cache *cache, const void *q, const int32_t *page_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+                                         int32_t batch, int32_t q_len, int32_t n_heads, int32_t n_kv_heads,
+                                         int32_t head_dim, float sm_scale, void *workspace, size_t workspace_bytes,
+                                         void *out, uint64_t page_wait_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEMRA_TESTING_H */

@@ -22,9 +22,14 @@ def memra():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(memra_[a-z0-9_]+)\s*\(", text)))
+    """Every function declared in include/*.h."""
+    names = set()
+    inc = os.path.dirname(HEADER)
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(memra_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported(memra):
@@ -115,6 +120,10 @@ def test_host_validation_without_gpu(memra):
     assert _decode(memra, c, Hq=258) == 2                               # group 129 > MEMRA_MAX_GROUP
     assert _decode(memra, c, B=65536) == 2                              # grid z limit
     assert L.memra_read_status(None, None, None) == 1
+    # the test hook of the bounded waits checks its limit before anything else
+    for bad_ns in (0, 10 ** 9 + 1):
+        assert L.memra_testing_decode_attn_short_page(ctypes.byref(c), 4096, 4096, 4, 4096, 64, 1, 1, 8, 2, 128,
+                                                      0.1, 4096, 1 << 20, 4096, bad_ns, None) == 1
     assert memra.status_string(3) == "workspace too small"
     assert memra.status_string(99) == "unknown status"
 
