@@ -786,18 +786,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
   grid_dependency_wait();          // q, the pools and the tables are written
   allow_dependent_launch();
 
-  for (int i = tid; i < nck * NPG; i += kWsThreads) {
-    const int tok = c0 * NC + i * kPage;
-    int pid = -1;
-    if (tok < p.prefix_len) {
-      pid = p.page_table[tok / kPage];
-      if (pid < 0 || pid >= p.num_pages) {
-        flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
-        pid = -1;
-      }
-    }
-    pid_s[i] = pid;
-  }
+  // the Q tile's loads first: their latency overlaps the page-id reads
   uint4 qv[QIT];
   if (tid < 256) {
 #pragma unroll
@@ -813,6 +802,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) cascade_prefix_ws_kernel(const 
         qv[it] = *reinterpret_cast<const uint4 *>(p.q + rowid * D + 8 * u);
       }
     }
+  }
+  for (int i = tid; i < nck * NPG; i += kWsThreads) {
+    const int tok = c0 * NC + i * kPage;
+    int pid = -1;
+    if (tok < p.prefix_len) {
+      pid = p.page_table[tok / kPage];
+      if (pid < 0 || pid >= p.num_pages) {
+        flag_error(p.status, MEMRA_DEVERR_BAD_PAGE);
+        pid = -1;
+      }
+    }
+    pid_s[i] = pid;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1182,63 +1183,70 @@ __global__ void __launch_bounds__(kThreads) cascade_combine_kernel(const Cascade
     return k < p.n_parts ? p.o_pre + (static_cast<size_t>(row) * p.n_parts + k) * D
                          : p.o_suf + (static_cast<size_t>(row) * p.nsplit_max + (k - p.n_parts)) * D;
   };
-  float m = -INFINITY;
-  for (int k = threadIdx.x; k < parts; k += kThreads) m = fmaxf(m, lse_of(k));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) mx[warp] = m;
-  __syncthreads();
-  float M = mx[0];
-#pragma unroll
-  for (int w = 1; w < W; ++w) M = fmaxf(M, mx[w]);
+  // One pass: warp w takes parts w, w + W, ..., eight in flight at a time,
+  // their lse and rows loaded together, and keeps a running maximum (its
+  // partial sums rescaled when it moves).  A part with lse = -inf (no keys, or
+  // a CTA that gave up) is never weighed: its row may hold anything.
+  float mw = -INFINITY, L = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    // warp w takes parts w, w + W, ...: eight of them in flight at a time
-    constexpr int BATCH = 8;
-    for (int k0 = warp; k0 < parts; k0 += BATCH * W) {
-      float ls[BATCH];
-      float4 x[BATCH][PER / 4];
+  constexpr int BATCH = 8;
+  for (int k0 = warp; k0 < parts; k0 += BATCH * W) {
+    float ls[BATCH];
+    float4 x[BATCH][PER / 4];
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const int k = k0 + u * W;
-        const bool in = k < parts;
-        ls[u] = in ? lse_of(k) : -INFINITY;
-        const float4 *src = reinterpret_cast<const float4 *>(o_of(in ? k : 0) + lane * PER);
+    for (int u = 0; u < BATCH; ++u) {
+      const int k = k0 + u * W;
+      const bool in = k < parts;
+      ls[u] = in ? lse_of(k) : -INFINITY;
+      const float4 *src = reinterpret_cast<const float4 *>(o_of(in ? k : 0) + lane * PER);
 #pragma unroll
-        for (int q4 = 0; q4 < PER / 4; ++q4) x[u][q4] = in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q4 = 0; q4 < PER / 4; ++q4) x[u][q4] = in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      if (ls[u] > mw) {
+        const float sc = fast_exp2(mw - ls[u]);      // 0 while mw = -inf
+        L *= sc;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] *= sc;
+        mw = ls[u];
       }
+      const float wgt = fast_exp2(ls[u] - mw);
+      L += wgt;
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        // a part with lse = -inf (no keys, or a CTA that gave up) is never
-        // weighed: its row may hold anything
-        if (ls[u] == -INFINITY) continue;
-        const float wgt = fast_exp2(ls[u] - M);
-        L += wgt;
-#pragma unroll
-        for (int q4 = 0; q4 < PER / 4; ++q4) {
-          acc[4 * q4 + 0] = fmaf(wgt, x[u][q4].x, acc[4 * q4 + 0]);
-          acc[4 * q4 + 1] = fmaf(wgt, x[u][q4].y, acc[4 * q4 + 1]);
-          acc[4 * q4 + 2] = fmaf(wgt, x[u][q4].z, acc[4 * q4 + 2]);
-          acc[4 * q4 + 3] = fmaf(wgt, x[u][q4].w, acc[4 * q4 + 3]);
-        }
+      for (int q4 = 0; q4 < PER / 4; ++q4) {
+        acc[4 * q4 + 0] = fmaf(wgt, x[u][q4].x, acc[4 * q4 + 0]);
+        acc[4 * q4 + 1] = fmaf(wgt, x[u][q4].y, acc[4 * q4 + 1]);
+        acc[4 * q4 + 2] = fmaf(wgt, x[u][q4].z, acc[4 * q4 + 2]);
+        acc[4 * q4 + 3] = fmaf(wgt, x[u][q4].w, acc[4 * q4 + 3]);
       }
     }
   }
 #pragma unroll
   for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
-  if (lane == 0) redl[warp] = L;
+  if (lane == 0) {
+    redl[warp] = L;
+    mx[warp] = mw;
+  }
   __syncthreads();
+  // the warps' sums, each scaled from its own maximum to the row's
+  float M = mx[0];
+#pragma unroll
+  for (int w = 1; w < W; ++w) M = fmaxf(M, mx[w]);
+  float wscale[W];
+#pragma unroll
+  for (int w = 0; w < W; ++w) wscale[w] = mx[w] == -INFINITY ? 0.f : fast_exp2(mx[w] - M);
   __half *dst = p.out + static_cast<size_t>(row) * D;
   for (int j = threadIdx.x; j < D / 2; j += kThreads) {
     float a0 = 0.f, a1 = 0.f, l = 0.f;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      a0 += red[w][2 * j];
-      a1 += red[w][2 * j + 1];
-      l += redl[w];
+      a0 = fmaf(wscale[w], red[w][2 * j], a0);
+      a1 = fmaf(wscale[w], red[w][2 * j + 1], a1);
+      l = fmaf(wscale[w], redl[w], l);
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     reinterpret_cast<__half2 *>(dst)[j] = __floats2half2_rn(a0 * inv, a1 * inv);

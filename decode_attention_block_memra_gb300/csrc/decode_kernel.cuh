@@ -206,6 +206,11 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   // merge launched after this grid sees both; the other CTAs leave as soon as
   // they are done and free their SM for the rest of the grid.
   if (p.skip == 0) grid_dependency_wait();
+  // The next launch (the combine, or a cascade call's merge) may start as soon
+  // as every CTA of this grid has started: its CTAs take the SMs this grid
+  // frees and wait on the device for this grid to complete, so its launch
+  // latency overlaps this grid's work.
+  allow_dependent_launch();
   const bool waits_for_prefix = p.skip != 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
   // This CTA: query position qi of sequence b and query heads 8 hg .. 8 hg + 7
@@ -899,7 +904,6 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
     }
   }
   if (waits_for_prefix) grid_dependency_wait();
-  allow_dependent_launch();
 }
 
 // One dispatcher per translation unit (head_dim).
