@@ -223,7 +223,12 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
   const memra_kv_cache &c = *a.cache;
   Plan pl;
   const int group = a.n_heads / a.n_kv_heads;
-  // a cascade call's own-key pass shares each SM with the prefix pass's CTAs
+  // A cascade call's own-key pass runs beside the prefix pass: where a CTA
+  // with the pass's shallowest pipeline fits an SM beside a prefix CTA, its
+  // shared memory is capped to that room, so that both share the SM.  Where
+  // none fits (the warp-specialized head_dim 128 prefix CTA fills its SM),
+  // the own-key CTAs run on the other SMs and keep the full pipeline: capped,
+  // they would hold one page per warp and wait a memory round trip per page.
   size_t cap = 0;
   if (a.prefix > 0) {
     int cpc = 1;
@@ -234,6 +239,10 @@ int run_partials(const DecodeArgs &a, const void *k_new, const void *v_new, cuda
                                         a.head_dim, k_seg_bytes(c.k_fmt, a.head_dim), v_seg_bytes(c.v_fmt, a.head_dim), cpc));
     const size_t used = kSmReservedPerCta * (1 + pre_per_sm) + pre;
     cap = used < kSmPerSm ? kSmPerSm - used : 1;
+    Plan smallest;
+    int rc1 = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &smallest, 1);
+    if (rc1) return rc1;
+    if (smallest.smem > cap) cap = 0;
   }
   int rc = make_plan(a.head_dim, c.k_fmt, c.v_fmt, a.q_len, group, a.max_seq_len, &pl, cap);
   if (rc) return rc;
