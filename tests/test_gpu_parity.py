@@ -738,3 +738,49 @@ def test_large_query_verify_rows_equal_plain_decode():
     w = _large_query_case(612, "q8_0", "q5_1", 128, q_len=4, heads_scaled=[0, 5, 6, 7, 12])
     out = _verify_vs_decode(w, fused=True)
     assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
+
+
+# ----------------------------------------------------- the header's maximums --
+# q_len up to MEMRA_MAX_Q_LEN (16: 15 drafts), groups up to MEMRA_MAX_GROUP
+# (128 query heads on one KV head), and splits clamped at
+# MEMRA_SPLIT_TOKENS_MAX (8,192 tokens) when T / S passes it.
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_maximum_q_len(D):
+    w = W.make_workload("max_qlen", batch=3, q_len=16, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=160 + D, seq_lens=[16, 1030, 2100], permute_pages=True, extra_pages=2)
+    res = run_fused(w)
+    assert res.flags == 0
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
+
+
+def test_maximum_q_len_verify_rows_equal_plain_decode():
+    K = 15
+    w = W.make_workload("verify_k15", batch=3, q_len=K + 1, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=215, seq_lens=[2051 + K, 1024 + 8, K + 1], permute_pages=True,
+                        extra_pages=2)
+    out = _verify_vs_decode(w, fused=True)
+    assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
+
+
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_maximum_group(q_len):
+    # 128 query heads on one KV head: 16 CTAs of 8 heads per position and split
+    w = W.make_workload("max_group", batch=2, q_len=q_len, n_heads=128, n_kv_heads=1, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q5_1", seed=128 + q_len, seq_lens=[q_len + 300, 2500], permute_pages=True)
+    res = run_fused(w)
+    assert res.flags == 0
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
+
+
+def test_splits_at_the_largest_split_size():
+    import decode_attention_block_memra_gb300 as memra
+    n_kv = 32
+    S = max(1, torch.cuda.get_device_properties(0).multi_processor_count * 2 // n_kv)
+    T = 80_000
+    assert -(-T // S) > memra.SPLIT_TOKENS and -(-T // S) > 8192     # T / S passes the 8,192-token clamp
+    w = W.make_workload("split_cap", batch=1, q_len=2, n_heads=32, n_kv_heads=n_kv, head_dim=128, k_fmt="q8_0",
+                        v_fmt="q4_0", seed=8192, seq_lens=[T], permute_pages=True)
+    res = run_fused(w)
+    assert res.flags == 0
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
