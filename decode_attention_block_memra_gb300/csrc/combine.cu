@@ -8,7 +8,8 @@
 // each lane owning D/32 consecutive outputs, so every split's partial is one
 // coalesced 512 B (D 128) or 1 KiB (D 256) read; the warps then reduce
 // through shared memory.  Launched as a programmatic dependent of the split
-// kernel, so its launch overlaps the split kernel's tail.
+// kernel, whose CTAs allow it as soon as they have started, so its launch
+// overlaps the split kernel's work.
 #include <cuda_runtime.h>
 
 #include "decode_kernel.cuh"
