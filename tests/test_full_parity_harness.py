@@ -45,3 +45,18 @@ def test_catches_one_output_element(case):
     bad[2, 1, 7, 100] = np.float16(np.inf)
     with pytest.raises(AssertionError, match="non-finite"):
         full_parity.check(w, bad)
+
+
+def test_ring_workload():
+    # sliding window over ring page tables: the harness reads each sequence's rows through its ring
+    w = W.make_window_workload("harness_ring", batch=2, q_len=2, n_heads=8, n_kv_heads=2, head_dim=128,
+                               k_fmt="q8_0", v_fmt="q4_0", seed=9, seq_lens=[70, 400], window=100,
+                               permute_pages=True, extra_pages=1)
+    kp, vp = attention.build_pools(w)
+    out = attention.reference(w).astype(np.float16)
+    s = full_parity.check(w, out, kp, vp, pages_per_piece=3)
+    assert s["rows"] == w.batch * w.q_len * w.n_heads
+    bad = out.copy()
+    bad[1, 0, 3, 5] += np.float16(0.01)
+    with pytest.raises(AssertionError, match="max"):
+        full_parity.check(w, bad, kp, vp, pages_per_piece=3)
