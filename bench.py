@@ -636,6 +636,7 @@ def main():
     e2e_total = max_over_ranks(sum(e2e_ms) / 1e3, world, "cuda")
     e2e_value = job_throughput(tokens_per_step, args.steps, world, e2e_total)
 
+    launches_per_step = b.launches_per_step
     per_workload = None
     if rank == 0 and not args.no_per_workload:
         del b, dw
@@ -665,7 +666,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_total / args.steps * 1e3},
             # per timed step: split-K (rows stored inside) + combine, or append + split-K + combine
-            "gpu_launches": b_launches(args, w, memra) * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "step_form": ("cascade " if args.cascade else "") + (
                 "two-call (memra_kv_append + memra_decode_attn)" if args.two_call else "fused (memra_decode_step)"),
             "clocks": clocks,
@@ -676,12 +677,6 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-def b_launches(args, w, memra) -> int:
-    """Kernel launches of one timed step (see Bench.launches_per_step)."""
-    combine = 1 if (args.cascade or w.max_seq_len > memra.SPLIT_TOKENS) else 0
-    return 1 + combine + (1 if args.two_call else 0) + (1 if args.cascade else 0)
 
 
 if __name__ == "__main__":
