@@ -12,7 +12,8 @@
 // The rules round exact real quotients, so the arithmetic is exact in float32
 // (GB300's float64 rate is far too low for a hot path): x - m is carried as an
 // unevaluated pair hi + lo (Knuth's TwoSum), a candidate rounding comes from
-// one float32 division, and the candidate is then confirmed or moved by one
+// a multiplication by the divisor's reciprocal (no IEEE division: a warp
+// spends ~200 cycles on each), and the candidate is then confirmed or moved by one
 // step by testing the sign of (hi - k*mid) + lo against the neighbouring
 // rounding midpoints mid, where k*mid and hi - k*mid are exact (few
 // significant bits; Sterbenz's lemma) and the final addition keeps the sign of

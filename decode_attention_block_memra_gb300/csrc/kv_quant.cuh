@@ -36,36 +36,49 @@ __device__ __forceinline__ void two_diff(float a, float b, float &hi, float &lo)
 }
 
 // fp16 round-to-nearest-even of (hi + lo) / k for hi + lo >= 0 and k in {7, 31, 127}.
+// The candidate is the fp16 rounding of hi * fp32(1/k): within one fp16 step
+// of the answer, since hi * fp32(1/k) is within 2^-22 (relative) of the
+// quotient.  The sign of (hi + lo) / k minus each neighbouring midpoint then
+// decides one step up or down, exactly: k times an fp16 midpoint has at most
+// 19 significant bits, and hi minus it is exact by Sterbenz's lemma.  No
+// branches: a warp's lanes never diverge here.
 __device__ __forceinline__ __half fp16_quotient_rne(float hi, float lo, float k) {
-  unsigned short hb = __half_as_ushort(__float2half_rn(__fdiv_rn(hi, k)));
-  const float v = __half2float(__ushort_as_half(hb));
+  const float inv_k = k == 127.f ? 1.f / 127.f : (k == 31.f ? 1.f / 31.f : 1.f / 7.f);
+  const unsigned hb = __half_as_ushort(__float2half_rn(__fmul_rn(hi, inv_k)));
+  const float v = __half2float(__ushort_as_half(static_cast<unsigned short>(hb)));
   const float up_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb + 1))));
+  const float dn_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb > 0 ? hb - 1 : 0))));
   const float t_up = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, up_mid)), lo);     // sign of x/k - up_mid
-  if (t_up > 0.f || (t_up == 0.f && (hb & 1))) {
-    ++hb;
-  } else if (hb > 0) {
-    const float dn_mid = 0.5f * (v + __half2float(__ushort_as_half(static_cast<unsigned short>(hb - 1))));
-    const float t_dn = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, dn_mid)), lo);
-    if (t_dn < 0.f || (t_dn == 0.f && (hb & 1))) --hb;
-  }
-  return __ushort_as_half(hb);
+  const float t_dn = __fadd_rn(__fsub_rn(hi, __fmul_rn(k, dn_mid)), lo);     // sign of x/k - dn_mid
+  const bool odd = hb & 1u;
+  const bool up = t_up > 0.f || (t_up == 0.f && odd);
+  const bool dn = !up && hb > 0 && (t_dn < 0.f || (t_dn == 0.f && odd));
+  return __ushort_as_half(static_cast<unsigned short>(hb + (up ? 1 : 0) - (dn ? 1 : 0)));
 }
 
+// Reciprocal of a block scale for quant_code's candidate (any value within a
+// few ulps of 1/d serves; 1 for d == 0, whose codes are 0).
+__device__ __forceinline__ float scale_reciprocal(float d) { return __fdividef(1.f, d == 0.f ? 1.f : d); }
+
 // clamp(rne((hi + lo) / d), lo_q, hi_q) for the stored fp16 d (as float); 0 when d == 0.
-__device__ __forceinline__ int quant_code(float hi, float lo, float d, int lo_q, int hi_q) {
-  if (d == 0.f) return 0;
-  float q0 = rintf(__fdiv_rn(hi, d));
-  const float e = __fsub_rn(hi, __fmul_rn(q0, d));          // exact
+// rd = scale_reciprocal(d).  The candidate is hi * rd rounded to the nearest
+// integer by adding 1.5 * 2^23 (float32 rounding is to nearest even, and the
+// integer then sits in the low mantissa bits): within one of the answer,
+// since |hi / d| < 2^8.  q0 * d is exact (8 + 11 significant bits) and so is
+// hi - q0 * d (Sterbenz); the signs of x/d - (q0 +- 1/2) then pick the code,
+// ties to even.  No branches.
+__device__ __forceinline__ int quant_code(float hi, float lo, float d, float rd, int lo_q, int hi_q) {
+  constexpr float kRound = 12582912.f;                           // 1.5 * 2^23
+  const float t = __fadd_rn(__fmul_rn(hi, rd), kRound);
+  int q = __float_as_int(t) - __float_as_int(kRound);
+  const float q0 = __fsub_rn(t, kRound);                         // exact
+  const float e = __fsub_rn(hi, __fmul_rn(q0, d));               // exact
   const float hd = 0.5f * d;
-  const float up = __fadd_rn(__fsub_rn(e, hd), lo);          // sign of x/d - (q0 + 1/2)
-  const int odd = static_cast<int>(q0) & 1;
-  if (up > 0.f || (up == 0.f && odd)) {
-    q0 += 1.f;
-  } else {
-    const float dn = __fadd_rn(__fadd_rn(e, hd), lo);        // sign of x/d - (q0 - 1/2)
-    if (dn < 0.f || (dn == 0.f && odd)) q0 -= 1.f;
-  }
-  return min(max(static_cast<int>(q0), lo_q), hi_q);
+  const float up = __fadd_rn(__fsub_rn(e, hd), lo);              // sign of x/d - (q0 + 1/2)
+  const float dn = __fadd_rn(__fadd_rn(e, hd), lo);              // sign of x/d - (q0 - 1/2)
+  const bool odd = q & 1;
+  q += (up > 0.f || (up == 0.f && odd)) ? 1 : ((dn < 0.f || (dn == 0.f && odd)) ? -1 : 0);
+  return d == 0.f ? 0 : min(max(q, lo_q), hi_q);
 }
 
 // NVFP4 codes of this lane's 8 elements (one half of a 16-element block; the
@@ -147,10 +160,10 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xk[i]));
       amax = group4_max(amax);
       const __half dh = fp16_quotient_rne(amax, 0.f, 127.f);
-      const float d = __half2float(dh);
+      const float d = __half2float(dh), rd = scale_reciprocal(d);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        code[i] = static_cast<uint8_t>(quant_code(xk[i], 0.f, d, -127, 127) + 128);   // stored biased
+        code[i] = static_cast<uint8_t>(quant_code(xk[i], 0.f, d, rd, -127, 127) + 128);   // stored biased
       if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
     } else {
 #pragma unroll
@@ -212,12 +225,12 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
         two_diff(mx, mn, rh, rl);
         dh = fp16_quotient_rne(rh, rl, 31.f);
         mh = __float2half_rn(mn);                      // exact: mn is an fp16 value
-        const float d = __half2float(dh);
+        const float d = __half2float(dh), rd = scale_reciprocal(d);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float xh, xl;
           two_diff(xv[i], mn, xh, xl);
-          q[i] = quant_code(xh, xl, d, 0, 31);
+          q[i] = quant_code(xh, xl, d, rd, 0, 31);
         }
       } else {  // q4_0, nibble = q + 8
         float amax = 0.f;
@@ -225,9 +238,9 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xv[i]));
         amax = group4_max(amax);
         dh = fp16_quotient_rne(amax, 0.f, 7.f);
-        const float d = __half2float(dh);
+        const float d = __half2float(dh), rd = scale_reciprocal(d);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], 0.f, d, -8, 7) + 8;
+        for (int i = 0; i < 8; ++i) q[i] = quant_code(xv[i], 0.f, d, rd, -8, 7) + 8;
       }
       // low nibbles: one byte per (vg, h) holding s = 0 (low) and s = 1 (high)
       if (act) {
