@@ -184,7 +184,7 @@ def workload_config(w) -> dict:
     """The workload a line measures (the same dict in the native and the oracle arm)."""
     return {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "context_tokens": int(w.seq_lens.sum()), "unique_tokens": int(w.slots.size),
-            "kv_format": f"{w.k_fmt}/{w.v_fmt}", "page_size": 16, "split_tokens": "max(1024, T / (SMs x CTAs per SM / KV heads))",
+            "kv_format": f"{w.k_fmt}/{w.v_fmt}", "page_size": 16, "split_tokens": "max(1280, T / (SMs x CTAs per SM / KV heads))",
             "l2": "flushed between steps (256 MiB write, then read back, outside the timed events)"}
 
 

@@ -16,7 +16,7 @@ from . import _build
 
 FORMATS = {"q8_0": 0, "q5_1": 1, "q4_0": 2, "fp8": 3, "nvfp4": 4}
 PAGE_SIZE = 16
-SPLIT_TOKENS = 1024
+SPLIT_TOKENS = 1280
 
 DEVERR_BAD_PAGE = 1
 DEVERR_BAD_SLOT = 2

@@ -23,8 +23,8 @@ constexpr int kSplitPagesMax = kSplitTokensMax / kPage;
 constexpr int kCascadeSplitTokens = 512;
 
 // Split size of a range of T tokens: enough splits to give one long sequence
-// `target` CTAs per KV head, never below `min_tokens` (1024; 256 for a cascade
-// call's own keys) or above 8192 tokens, a multiple of the page.  Depends on T
+// `target` CTAs per KV head, never below `min_tokens` (MEMRA_SPLIT_TOKENS; 512
+// for a cascade call's own keys) or above 8192 tokens, a multiple of the page.  Depends on T
 // and the device only.
 __host__ __device__ __forceinline__ int split_tokens(int T, int target, int min_tokens) {
   const int t = target > 0 ? target : 1;

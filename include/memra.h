@@ -123,13 +123,17 @@ typedef enum {
  * device) x (CTAs per SM of the kernel configuration) / n_kv_heads, so that one
  * long sequence fills the GPU in one wave.  C depends only on the sequence's
  * own length and the device, never on the rest of the batch: a sequence's
- * result bytes are the same alone or batched. */
+ * result bytes are the same alone or batched.  The floor of 1,280 tokens
+ * (measured against 1,024 to 2,048 on batch-1 decode from 8K to 256K tokens,
+ * batches of 4 to 64, verify and shared prefixes) keeps the per-split fixed
+ * cost small where many sequences fill the GPU, without slowing a single
+ * sequence of moderate length. */
 #define MEMRA_PAGE_SIZE 16
 /* Largest q_len (new tokens per sequence: 1 + draft tokens) and largest GQA
  * group n_heads / n_kv_heads that the decode calls take. */
 #define MEMRA_MAX_Q_LEN 16
 #define MEMRA_MAX_GROUP 128
-#define MEMRA_SPLIT_TOKENS 1024
+#define MEMRA_SPLIT_TOKENS 1280
 #define MEMRA_SPLIT_TOKENS_MAX 8192
 
 /* A paged KV cache.  Plain data; the caller owns the pools and status word. */
@@ -169,9 +173,9 @@ int memra_kv_append(const memra_kv_cache *cache, const void *k, const void *v,
                     const int32_t *slot_mapping, int32_t n_tok, void *stream);
 
 /* Workspace bytes memra_decode_attn needs for these sizes (the split-K
- * partials: float32 [batch*q_len*n_heads][ceil(max_seq_len/1024)][head_dim]
- * plus one float32 log-sum-exp per partial; ceil(max_seq_len/1024) bounds the
- * split count of any sequence).  Host only. */
+ * partials: float32 [batch*q_len*n_heads][memra_num_splits(max_seq_len)][head_dim]
+ * plus one float32 log-sum-exp per partial; memra_num_splits(max_seq_len)
+ * bounds the split count of any sequence).  Host only. */
 size_t memra_decode_attn_workspace_bytes(int32_t batch, int32_t q_len, int32_t n_heads,
                                          int32_t head_dim, int32_t max_seq_len);
 
@@ -203,7 +207,7 @@ int memra_decode_attn(const memra_kv_cache *cache, const void *q, const int32_t 
 
 /* The two passes of memra_decode_attn, separately (same arguments and
  * meaning).  memra_decode_attn == partials followed by combine on one
- * stream (the combine is left out when max_seq_len <= 1024: every row then
+ * stream (the combine is left out when max_seq_len <= MEMRA_SPLIT_TOKENS: every row then
  * fits one split).  Rows that fit one split, and rows with no visible key
  * (zeros), are written to `out` by the partials pass directly; the combine
  * pass merges the others. */

@@ -65,10 +65,12 @@ def test_segment_and_pool_sizes(memra):
 def test_split_plan_and_workspace(memra):
     assert memra.num_splits(0) == 0
     assert memra.num_splits(1) == 1
-    assert memra.num_splits(1024) == 1
-    assert memra.num_splits(1025) == 2
-    assert memra.num_splits(262144) == 256
-    rows, ns, D = 1 * 1 * 32, 256, 128
+    C = memra.SPLIT_TOKENS
+    assert C == 1280
+    assert memra.num_splits(C) == 1
+    assert memra.num_splits(C + 1) == 2
+    assert memra.num_splits(262144) == 205
+    rows, ns, D = 1 * 1 * 32, 205, 128
     o = rows * ns * D * 4
     assert memra.decode_attn_workspace_bytes(1, 1, 32, 128, 262144) == ((o + 255) // 256) * 256 + rows * ns * 4
     assert memra.decode_attn_workspace_bytes(4, 1, 8, 128, 0) == 0

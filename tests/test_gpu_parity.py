@@ -20,6 +20,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
+C = 1280        # MEMRA_SPLIT_TOKENS: the smallest split (tests below place lengths around it)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,6 +31,7 @@ def built():
     _build.build()
     import decode_attention_block_memra_gb300 as memra
     memra.lib()
+    assert memra.SPLIT_TOKENS == C
 
 
 def run(w, fill_seed=1, want_pools=True):
@@ -100,7 +102,7 @@ def test_query_shapes(q_len, n_heads, n_kv_heads, D):
     assert_out_close(w, res, attention.reference(w))
 
 
-@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 511, 512, 513, 1023, 1024, 1025, 2049])
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 511, 512, 513, 1024, C - 1, C, C + 1, 2 * C + 1])
 def test_context_edges(T):
     w = W.make_workload(f"edge{T}", batch=1, q_len=1, n_heads=8, n_kv_heads=1, head_dim=128, k_fmt="q8_0",
                         v_fmt="q5_1", seed=T, seq_lens=[T], permute_pages=True, extra_pages=2)
@@ -119,7 +121,7 @@ def test_context_edges(T):
 def test_causal_verify_rows_start_mid_page():
     # q_len 6 with the new rows crossing a page and a split boundary
     w = W.make_workload("verify_cross", batch=2, q_len=6, n_heads=8, n_kv_heads=2, head_dim=128, k_fmt="q8_0",
-                        v_fmt="q5_1", seed=3, seq_lens=[1027, 1030])
+                        v_fmt="q5_1", seed=3, seq_lens=[C + 3, C + 6])
     res = run(w)
     assert res.flags == 0
     assert_out_close(w, res, attention.reference(w))
@@ -362,8 +364,8 @@ def test_fused_step_formats(kf, vf, D):
 
 @pytest.mark.parametrize("q_len,n_heads,n_kv_heads,D,seq_lens", [
     (1, 8, 1, 128, [1]),                  # the only key is the new one
-    (1, 8, 1, 128, [17, 16, 1025]),       # new row opens a page / closes a page / opens a split
-    (4, 32, 4, 128, [1026, 1030, 4]),     # verify rows cross the split boundary at 1,024; whole sequence new
+    (1, 8, 1, 128, [17, 16, C + 1]),      # new row opens a page / closes a page / opens a split
+    (4, 32, 4, 128, [C + 2, C + 6, 4]),   # verify rows cross the smallest split's boundary; whole sequence new
     (6, 8, 2, 128, [8000, 1027]),         # new rows deep in a long split (beyond the first ring fill)
     (8, 64, 8, 128, [700, 2049]),         # 64 rows per KV head
     (4, 16, 2, 256, [33, 1100]),          # D 256: 32 lanes per stored row
@@ -471,9 +473,9 @@ def _verify_vs_decode(w, fused):
 @pytest.mark.parametrize("K", range(1, 9))
 def test_verify_rows_equal_plain_decode(K):
     Q = K + 1
-    # contexts: ragged, crossing the 1,024-token split boundary inside the
-    # verify window, one split, and a sequence made only of new tokens
-    seq_lens = [2051 + K, 1024 + Q // 2, 300 + K, Q]
+    # contexts: ragged, crossing a split boundary inside the verify window,
+    # one split, and a sequence made only of new tokens
+    seq_lens = [2 * C + 3 + K, C + Q // 2, 300 + K, Q]
     w = W.make_workload(f"verify_k{K}", batch=4, q_len=Q, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
                         v_fmt="q5_1", seed=40 + K, seq_lens=seq_lens, permute_pages=True, extra_pages=2)
     out = _verify_vs_decode(w, fused=(K % 2 == 0))
@@ -487,7 +489,7 @@ def test_verify_rows_equal_plain_decode_across_split_size_step(K, D, kf, vf):
     Q = K + 1
     n_kv_heads = 32
     S = max(1, torch.cuda.get_device_properties(0).multi_processor_count * 2 // n_kv_heads)
-    t_step = S * 16 * 64 + 1              # first length whose ceil(T / S) passes 1,024 (C: 1,024 -> 1,040)
+    t_step = S * C + 1                    # first length whose ceil(T / S) passes C (C(T): 1,280 -> 1,296)
     seq_lens = [t_step + Q // 2, t_step + Q - 1]
     w = W.make_workload("verify_cstep", batch=2, q_len=Q, n_heads=n_kv_heads, n_kv_heads=n_kv_heads, head_dim=D,
                         k_fmt=kf, v_fmt=vf, seed=90 + K, seq_lens=seq_lens)
@@ -515,7 +517,7 @@ def test_window_formats(kf, vf, D):
     (1, 1, [1, 17, 500]),            # each row sees only itself
     (16, 4, [16, 20, 333]),          # window of one page
     (1000, 4, [999, 1000, 1001, 5000]),
-    (1500, 2, [4097, 2050]),         # splits of a window range (C = 1,024), window start mid-page
+    (1500, 2, [4097, 2050]),         # splits of a window range (C = 1,280), window start mid-page
     (4096, 8, [262144]),             # an SWA layer of a 262,144-token session: a 258-page ring
 ])
 def test_window_shapes(window, q_len, seq_lens):
@@ -532,7 +534,7 @@ def test_window_shapes(window, q_len, seq_lens):
 def test_window_verify_rows_equal_plain_decode(K):
     Q = K + 1
     w = W.make_window_workload(f"win_verify{K}", batch=3, q_len=Q, n_heads=32, n_kv_heads=4, head_dim=128,
-                               k_fmt="q8_0", v_fmt="q5_1", seed=70 + K, seq_lens=[3000 + K, 1030, Q], window=1025,
+                               k_fmt="q8_0", v_fmt="q5_1", seed=70 + K, seq_lens=[3000 + K, C + 6, Q], window=C + 1,
                                permute_pages=True)
     from decode_attention_block_memra_gb300.runner import upload
     import decode_attention_block_memra_gb300 as memra
@@ -615,7 +617,7 @@ def test_nvfp4_full_size_long_context():
 @pytest.mark.parametrize("kf,vf,D", [("fp8", "q4_0", 128), ("nvfp4", "nvfp4", 128), ("q8_0", "fp8", 256)])
 def test_verify_rows_equal_plain_decode_other_formats(kf, vf, D):
     w = W.make_workload("verify_fmt", batch=3, q_len=4, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt=kf, v_fmt=vf,
-                        seed=77 + D, seq_lens=[2051, 1026, 300], permute_pages=True, extra_pages=1)
+                        seed=77 + D, seq_lens=[2 * C + 3, C + 2, 300], permute_pages=True, extra_pages=1)
     out = _verify_vs_decode(w, fused=True)
     assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
 
@@ -748,7 +750,7 @@ def test_large_query_verify_rows_equal_plain_decode():
 @pytest.mark.parametrize("D", [128, 256])
 def test_maximum_q_len(D):
     w = W.make_workload("max_qlen", batch=3, q_len=16, n_heads=16, n_kv_heads=2, head_dim=D, k_fmt="q8_0",
-                        v_fmt="q5_1", seed=160 + D, seq_lens=[16, 1030, 2100], permute_pages=True, extra_pages=2)
+                        v_fmt="q5_1", seed=160 + D, seq_lens=[16, C + 6, 2100], permute_pages=True, extra_pages=2)
     res = run_fused(w)
     assert res.flags == 0
     full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
@@ -757,7 +759,7 @@ def test_maximum_q_len(D):
 def test_maximum_q_len_verify_rows_equal_plain_decode():
     K = 15
     w = W.make_workload("verify_k15", batch=3, q_len=K + 1, n_heads=32, n_kv_heads=4, head_dim=128, k_fmt="q8_0",
-                        v_fmt="q5_1", seed=215, seq_lens=[2051 + K, 1024 + 8, K + 1], permute_pages=True,
+                        v_fmt="q5_1", seed=215, seq_lens=[2 * C + 3 + K, C + 8, K + 1], permute_pages=True,
                         extra_pages=2)
     out = _verify_vs_decode(w, fused=True)
     assert_out_close(w, SimpleNamespace(out=out), attention.reference(w))
