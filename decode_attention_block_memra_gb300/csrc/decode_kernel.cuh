@@ -393,26 +393,30 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
 
   if (app_n > 0) {
     // Fused append: quantize this KV head's rows of the new tokens into their
-    // pool pages (one row per D/8 lanes, the same code as the append kernel),
-    // then order those generic stores before the bulk copies that read them.
+    // pool pages (one row side per D/8 lanes, the same code as the append
+    // kernel; even warps take the K rows and odd warps the V rows, so the two
+    // sides run in parallel), then order those generic stores before the bulk
+    // copies that read them.
     constexpr int kLanesRow = D / 8;
-    constexpr int kRowsPass = kThreads / kLanesRow;
+    constexpr int kRowsWarp = 32 / kLanesRow;
+    constexpr int kRowsPass = (kWarps / 2) * kRowsWarp;
     const QuantTarget dst{const_cast<uint8_t *>(p.k_pool), const_cast<uint8_t *>(p.v_pool), p.n_kv_heads, KF, VF,
                           p.k_scale, p.v_scale};
-    const int l = tid % kLanesRow;
+    const int l = lane % kLanesRow;
+    const bool v_side = warp & 1;            // warp-uniform
+    const __half *src = v_side ? p.v_new : p.k_new;
     const int first_new = Tseq - p.q_len;    // position of new token 0
     for (int j0 = 0; j0 < app_n; j0 += kRowsPass) {
-      const int j = j0 + tid / kLanesRow;
+      const int j = j0 + (warp >> 1) * kRowsWarp + lane / kLanesRow;
       const int pos = app_pos0 + j;
       int page = -1;
-      uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+      uint4 rx = make_uint4(0, 0, 0, 0);
       if (j < app_n) {
         page = pid_s[pos / kPage - tok0 / kPage];
         const size_t off = ((static_cast<size_t>(b) * p.q_len + (pos - first_new)) * p.n_kv_heads + kvh) * D + 8 * l;
-        rk = *reinterpret_cast<const uint4 *>(p.k_new + off);
-        rv = *reinterpret_cast<const uint4 *>(p.v_new + off);
+        rx = *reinterpret_cast<const uint4 *>(src + off);
       }
-      quantize_store_row<D>(dst, page >= 0, max(page, 0), pos % kPage, kvh, l, rk, rv);
+      quantize_store_row<D>(dst, page >= 0, max(page, 0), pos % kPage, kvh, l, rx, rx, !v_side, v_side);
     }
     fence_proxy_async_global();
     __syncthreads();

@@ -106,11 +106,14 @@ __device__ __forceinline__ uint32_t nvfp4_half_block(const float (&x)[8], float 
 
 // One (token, KV head) row per group of D/8 consecutive lanes; lane l of the
 // group holds elements 8l..8l+7 of the K row (rk) and of the V row (rv).
-// Every lane of the warp must call it (it shuffles within the group); only
-// rows with act set are stored, at token t of pool page `page`.
+// Every lane of the warp must call it, with the same do_k / do_v (it shuffles
+// within the group); only rows with act set are stored, at token t of pool
+// page `page`.  do_k / do_v select the sides to quantize (a caller may give K
+// and V of a row to different warps, which then run in parallel).
 template <int D>
 __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool act, int page, int t, int head,
-                                                   int l, uint4 rk, uint4 rv) {
+                                                   int l, uint4 rk, uint4 rv, bool do_k = true,
+                                                   bool do_v = true) {
   constexpr int kNb = D / 32;
   const int b = l / 4;                            // block
   const int cc = l % 4;                           // 8-element chunk within the block
@@ -134,7 +137,8 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
   }
 
   // ------------------------------------------------------------------ K ---
-  if (dst.k_fmt == MEMRA_KV_NVFP4) {
+  if (!do_k) {
+  } else if (dst.k_fmt == MEMRA_KV_NVFP4) {
     uint8_t *seg = dst.k_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * k_seg_bytes(dst.k_fmt, D);
     uint32_t code[8];
     const uint32_t sb = nvfp4_half_block(xk, dst.k_scale, code);
@@ -179,7 +183,8 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
   }
 
   // ------------------------------------------------------------------ V ---
-  if (dst.v_fmt == MEMRA_KV_NVFP4) {
+  if (!do_v) {
+  } else if (dst.v_fmt == MEMRA_KV_NVFP4) {
     uint8_t *seg = dst.v_pool + (static_cast<size_t>(page) * dst.n_kv_heads + head) * v_seg_bytes(dst.v_fmt, D);
     uint32_t code[8];
     const uint32_t sb = nvfp4_half_block(xv, dst.v_scale, code);
