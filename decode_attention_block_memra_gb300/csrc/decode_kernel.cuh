@@ -246,6 +246,24 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
   const int R = kWarps;                         // page lanes: warp r takes pages r, r + R, ...
   const int r = warp;
 
+  const int g = lane >> 2, c = lane & 3;
+  // The query's loads go out first: their latency overlaps the page-table reads.
+  // Q^T fragments (B operand of S^T = K^ Q^T): row g, dims 32bb+8c..+7.
+  uint4 qf[NT][NB];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    if (g < nrows) {
+      const int head = kvh * p.group + 8 * hg + g;
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          p.q + ((static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head) * D + 8 * c);
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = src[4 * bb];
+    } else {
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
   {
     const int32_t *pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
     for (int i = tid; i < npages; i += kThreads) {
@@ -291,26 +309,9 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       if (i < app_lo || i > app_hi) issue(i, i);
   }
 
-  const int g = lane >> 2, c = lane & 3;
   // Q^T fragments live in shared memory (warp-private, fragment order: one
   // conflict-free 16-byte load per block), not in 16+ registers.
   const uint32_t qsm = smem_addr(smem + region + 16 * NS + 4 * kSplitPagesMax) + warp * (NT * NB * 512);
-
-  // Q^T fragments (B operand of S^T = K^ Q^T): row g, dims 32bb+8c..+7.
-  uint4 qf[NT][NB];
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    if (g < nrows) {
-      const int head = kvh * p.group + 8 * hg + g;
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          p.q + ((static_cast<size_t>(b) * p.q_len + qi) * p.n_heads + head) * D + 8 * c);
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = src[4 * bb];
-    } else {
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) qf[n][bb] = make_uint4(0, 0, 0, 0);
-    }
-  }
 
   // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q,
   // so block b's raw product is acc_b = sum_j q_j Q_j + 1152 sum_j Q_j.  The
