@@ -99,6 +99,8 @@ _SIGS = {
                                              [ctypes.c_int32] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                      ctypes.c_size_t, ctypes.c_void_p,
                                                                      ctypes.c_uint64, ctypes.c_void_p]),
+    "memra_testing_scale_division_mismatches": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                                ctypes.c_void_p]),
     "memra_read_status": (ctypes.c_int, [ctypes.POINTER(KVCacheStruct), ctypes.POINTER(ctypes.c_int32),
                                          ctypes.c_void_p]),
     "memra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -304,6 +306,13 @@ def testing_decode_attn_short_page(cache: KVCache, q, page_table, seq_lens, max_
     a = _decode_args(cache, q, page_table, seq_lens, max_seq_len, out, workspace, sm_scale)
     _check(lib().memra_testing_decode_attn_short_page(*a, int(page_wait_ns), _stream(stream)),
            "memra_testing_decode_attn_short_page")
+
+
+def testing_scale_division_mismatches(scales, mismatches, stream=None) -> None:
+    """memra_testing_scale_division_mismatches (memra_testing.h): adds to mismatches (one int64 on the device)
+    the (fp16 x, scale) pairs whose division-free quotient differs from the IEEE one."""
+    _check(lib().memra_testing_scale_division_mismatches(_ptr(scales), int(scales.numel()), _ptr(mismatches),
+                                                         _stream(stream)), "memra_testing_scale_division_mismatches")
 
 
 def read_status(cache: KVCache, stream=None) -> int:

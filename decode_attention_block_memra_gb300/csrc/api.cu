@@ -606,3 +606,26 @@ extern "C" int memra_testing_decode_attn_short_page(const memra_kv_cache *cache,
   return decode_both_passes(a, nullptr, nullptr, stream);
 }
 
+// memra_testing.h: the quantizer's division by a scale (kv_quant.cuh) against
+// the IEEE quotient, for every finite fp16 dividend and the given scales.
+namespace {
+__global__ void scale_division_check_kernel(const float *scales, unsigned long long *mismatches) {
+  const float s = scales[blockIdx.y];
+  const float r = __frcp_rn(s);
+  unsigned long long bad = 0;
+  for (int bits = blockIdx.x * blockDim.x + threadIdx.x; bits < 65536; bits += gridDim.x * blockDim.x) {
+    const float x = __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    if (!isfinite(x)) continue;
+    if (__float_as_uint(memra::div_by_scale(x, s, r)) != __float_as_uint(__fdiv_rn(x, s))) ++bad;
+  }
+  if (bad) atomicAdd(mismatches, bad);
+}
+}  // namespace
+
+extern "C" int memra_testing_scale_division_mismatches(const float *scales, int32_t n_scales,
+                                                       unsigned long long *mismatches, void *stream) {
+  if (!scales || !mismatches || n_scales < 1 || n_scales > 65535) return MEMRA_ERR_INVALID_ARG;
+  scale_division_check_kernel<<<dim3(16, static_cast<unsigned>(n_scales)), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      scales, mismatches);
+  return cudaGetLastError() == cudaSuccess ? MEMRA_OK : MEMRA_ERR_CUDA;
+}

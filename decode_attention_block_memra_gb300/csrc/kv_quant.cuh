@@ -81,6 +81,25 @@ __device__ __forceinline__ int quant_code(float hi, float lo, float d, float rd,
   return d == 0.f ? 0 : min(max(q, lo_q), hi_q);
 }
 
+// The IEEE float32 quotient RN(x / s) of an fp16 value x by a scale s, given
+// r = RN(1 / s), without a division: x * r is within two ulps of the
+// quotient, one refinement q + RN(x - q s) r brings it within one ulp, and a
+// second gives the correctly rounded quotient (Markstein's division
+// theorem: the remainder of a quotient within one ulp is exact, and
+// RN(q + (x - q s) r) = RN(x / s) for r = RN(1 / s)).  The fp8 and NVFP4
+// rules round this quotient, so it must be the IEEE one: a GPU test checks
+// it against __fdiv_rn for every finite fp16 x over thousands of scales.
+// Scales outside [2^-60, 2^60], where a remainder could leave the normal
+// range, take the IEEE division.  A warp spends ~200 cycles on each IEEE
+// division, a few on this.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  if (!(s >= 0x1p-60f && s <= 0x1p60f)) return __fdiv_rn(x, s);
+  const float q0 = __fmul_rn(x, r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+  const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
+  return x == 0.f ? q0 : q2;        // a zero keeps its sign
+}
+
 // NVFP4 codes of this lane's 8 elements (one half of a 16-element block; the
 // partner half is on lane l ^ 1): e4m3 block scale of max|x| / (6 s) and E2M1
 // codes of x / (scale * s), each step one float32 operation.  Returns the
@@ -90,14 +109,16 @@ __device__ __forceinline__ uint32_t nvfp4_half_block(const float (&x)[8], float 
 #pragma unroll
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  const float u = __fdiv_rn(amax, __fmul_rn(6.f, s));
+  const float s6 = __fmul_rn(6.f, s);
+  const float u = div_by_scale(amax, s6, __frcp_rn(s6));
   const uint32_t sb = __nv_cvt_float_to_fp8(u, __NV_SATFINITE, __NV_E4M3);
   const float eff = __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sb),
                                                                               __NV_E4M3))), s);
+  const float reff = __frcp_rn(sb != 0 ? eff : 1.f);
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
     uint32_t two = 0;
-    if (sb != 0) two = float2_to_e2m1x2(__fdiv_rn(x[i + 1], eff), __fdiv_rn(x[i], eff));
+    if (sb != 0) two = float2_to_e2m1x2(div_by_scale(x[i + 1], eff, reff), div_by_scale(x[i], eff, reff));
     codes[i] = two & 0xFu;
     codes[i + 1] = two >> 4;
   }
@@ -170,9 +191,10 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
         code[i] = static_cast<uint8_t>(quant_code(xk[i], 0.f, d, rd, -127, 127) + 128);   // stored biased
       if (act && cc == 0) store_half(seg + 16 * D + (t * kNb + b) * 2, dh);
     } else {
+      const float r = __frcp_rn(dst.k_scale);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        code[i] = __nv_cvt_float_to_fp8(__fdiv_rn(xk[i], dst.k_scale), __NV_SATFINITE, __NV_E4M3);
+        code[i] = __nv_cvt_float_to_fp8(div_by_scale(xk[i], dst.k_scale, r), __NV_SATFINITE, __NV_E4M3);
     }
     if (act) {
       uint2 w;
@@ -210,10 +232,11 @@ __device__ __forceinline__ void quantize_store_row(const QuantTarget &dst, bool 
     // element i of this lane: r = 8*cc + i -> vg = 2*cc + i/4, h = (i%4)/2, s = i%2
     if (dst.v_fmt == MEMRA_KV_FP8_E4M3) {
       if (act) {
+        const float r = __frcp_rn(dst.v_scale);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int vg = 2 * cc + i / 4, h = (i % 4) / 2, s = i % 2;
-          const uint8_t byte = __nv_cvt_float_to_fp8(__fdiv_rn(xv[i], dst.v_scale), __NV_SATFINITE, __NV_E4M3);
+          const uint8_t byte = __nv_cvt_float_to_fp8(div_by_scale(xv[i], dst.v_scale, r), __NV_SATFINITE, __NV_E4M3);
           seg[(b * 32 + 4 * vg + c) * 16 + 8 * h + 2 * (2 * pp + s) + f] = byte;
         }
       }

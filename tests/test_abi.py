@@ -126,6 +126,9 @@ def test_host_validation_without_gpu(memra):
     for bad_ns in (0, 10 ** 9 + 1):
         assert L.memra_testing_decode_attn_short_page(ctypes.byref(c), 4096, 4096, 4, 4096, 64, 1, 1, 8, 2, 128,
                                                       0.1, 4096, 1 << 20, 4096, bad_ns, None) == 1
+    assert L.memra_testing_scale_division_mismatches(None, 1, 4096, None) == 1
+    assert L.memra_testing_scale_division_mismatches(4096, 0, 4096, None) == 1
+    assert L.memra_testing_scale_division_mismatches(4096, 65536, 4096, None) == 1
     assert memra.status_string(3) == "workspace too small"
     assert memra.status_string(99) == "unknown status"
 
