@@ -76,8 +76,13 @@ __device__ __forceinline__ int quant_code(float hi, float lo, float d, float rd,
   const float hd = 0.5f * d;
   const float up = __fadd_rn(__fsub_rn(e, hd), lo);              // sign of x/d - (q0 + 1/2)
   const float dn = __fadd_rn(__fadd_rn(e, hd), lo);              // sign of x/d - (q0 - 1/2)
-  const bool odd = q & 1;
-  q += (up > 0.f || (up == 0.f && odd)) ? 1 : ((dn < 0.f || (dn == 0.f && odd)) ? -1 : 0);
+  // Sign tests on the bits (a float is > 0 iff its bits are > 0 as an int, and
+  // zero iff they are 0 after the sign bit): fewer predicates than float
+  // compares, so the eight codes of a lane interleave.  Up and down never both
+  // hold (dn exceeds up by d).
+  const int iu = __float_as_int(up), id = __float_as_int(dn), odd = q & 1;
+  const int zu = (iu << 1) == 0, zd = (id << 1) == 0;
+  q += ((iu > 0) | (zu & odd)) - (((id < 0) & !zd) | (zd & odd));
   return d == 0.f ? 0 : min(max(q, lo_q), hi_q);
 }
 
