@@ -81,16 +81,16 @@ size_t merge_bytes(int D) {
 // CTAs per (split, KV head, sequence) and pipeline depth.  Every query
 // position and every group of 8 query heads of a KV head gets its own CTA
 // (8 rows, one per MMA column), planned from the position's own length.
-// max_cta_smem caps the shared memory of one CTA (0: two CTAs per SM).
+// max_cta_smem caps the shared memory of one CTA (0: the kernel's CTAs per SM).
 int make_plan(int D, int kf, int vf, int q_len, int group, int max_seq_len, Plan *pl, size_t max_cta_smem = 0) {
   if (q_len > MEMRA_MAX_Q_LEN || group > MEMRA_MAX_GROUP) return MEMRA_ERR_UNSUPPORTED;
   const int W = warps_for(D);
   // Pipeline depth: as many 16-token pages in flight as fit beside the other
-  // CTA of the SM, in steps of the warp count so that page i and page
+  // CTAs of the SM, in steps of the warp count so that page i and page
   // i + depth meet the same warp.
   const size_t stage = static_cast<size_t>(k_seg_bytes(kf, D)) + v_seg_bytes(vf, D);
-  const int ctas_per_sm = 2;
-  const size_t qbytes = static_cast<size_t>(W) * (D / 32) * 512;     // warp-private Q fragments
+  const int ctas_per_sm = D == 128 ? kCtasPerSmFor<128> : kCtasPerSmFor<256>;
+  const size_t qbytes = static_cast<size_t>(D == 128 ? W : 1) * (D / 32) * 512;   // Q fragments (per warp at D 128)
   size_t cta = (226 * 1024) / ctas_per_sm;
   if (max_cta_smem && max_cta_smem < cta) cta = max_cta_smem;
   const size_t fixed = 2048 + qbytes + 4 * static_cast<size_t>(kSplitPagesMax);

@@ -17,7 +17,7 @@
 // The CTAs of one split's positions are neighbours in the grid and read the
 // same pages, so L2 serves all but the first read.
 //
-// How (one CTA = 8 warps at head_dim 128, 4 at 256, 2 CTAs per SM):
+// How (one CTA = 8 warps at head_dim 128, 2 CTAs per SM; 4 warps at 256, 3 per SM):
 //  * Warp w takes pages w, w + W, ... of the split, issues its own pages'
 //    copies (one contiguous bulk copy each for the K and V segments, 16-byte
 //    aligned, evict-first in L2) `num_stages` pages ahead into its own ring
@@ -100,9 +100,17 @@ cudaError_t launch_combine(int D, const CombineParams &p, cudaStream_t st);
 cudaError_t launch_kv_append(const memra_kv_cache &c, const void *k, const void *v, const int32_t *slots, int n_tok,
                              cudaStream_t stream);
 
-// Warps (page lanes) per CTA: 8 at head_dim 128, 4 at 256; 2 CTAs/SM.
+// Warps (page lanes) per CTA: 8 at head_dim 128, 4 at 256.
 template <int D>
 constexpr int kWarpsFor = D == 128 ? 8 : 4;
+// CTAs per SM the plan sizes shared memory and registers for: two 8-warp CTAs
+// at head_dim 128; three 4-warp CTAs at 256, whose warps share one copy of
+// the query fragments (12 warps per SM instead of 8 with two CTAs: the format
+// sweep's split kernel 170-184 against 188-205 us, same box).
+template <int D>
+constexpr int kCtasPerSmFor = D == 128 ? 2 : 3;
+template <int D>
+constexpr bool kSharedQFor = D == 256;
 
 template <int D>
 struct MergeLayout {
@@ -167,7 +175,7 @@ __device__ __forceinline__ uint32_t shift_const(uint32_t x) {
 }
 
 template <int D, int KF, int VF>
-__global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
+__global__ void __launch_bounds__(kWarpsFor<D> * 32, kCtasPerSmFor<D>)
     decode_split_kernel(const DecodeParams p) {
   constexpr int NT = 1;                       // one n-tile of 8 query rows
   constexpr int NB = D / 32;
@@ -309,9 +317,10 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
       if (i < app_lo || i > app_hi) issue(i, i);
   }
 
-  // Q^T fragments live in shared memory (warp-private, fragment order: one
-  // conflict-free 16-byte load per block), not in 16+ registers.
-  const uint32_t qsm = smem_addr(smem + region + 16 * NS + 4 * kSplitPagesMax) + warp * (NT * NB * 512);
+  // Q^T fragments live in shared memory (fragment order: one conflict-free
+  // 16-byte load per block), not in 16+ registers: warp-private at head_dim
+  // 128, one copy per CTA (written by warp 0) at 256.
+  const uint32_t qsm = smem_addr(smem + region + 16 * NS + 4 * kSplitPagesMax) + (kSharedQFor<D> ? 0 : warp * (NT * NB * 512));
 
   // q8_0 codes are stored biased (q + 128) and enter the MMA as fp16 1152 + q,
   // so block b's raw product is acc_b = sum_j q_j Q_j + 1152 sum_j Q_j.  The
@@ -386,11 +395,13 @@ __global__ void __launch_bounds__(kWarpsFor<D> * 32, 2)
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) {
       const uint4 v = qf[n][bb];
-      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qsm + ((n * NB + bb) * 32 + lane) * 16), "r"(v.x),
-                   "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+      if (!kSharedQFor<D> || warp == 0)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qsm + ((n * NB + bb) * 32 + lane) * 16), "r"(v.x),
+                     "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
     }
   }
-  __syncwarp();
+  if constexpr (kSharedQFor<D>) __syncthreads();
+  else __syncwarp();
 
   if (app_n > 0) {
     // Fused append: quantize this KV head's rows of the new tokens into their
