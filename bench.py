@@ -490,7 +490,10 @@ def summarize(w, step_ms, split_ms, peak, cascade=False) -> dict:
             "kv_bytes_unique": kv, "kv_bytes_logical": logical_kv_bytes(w),
             "kv_gbs_step": kv / step_s / 1e9,
             "split_kernel": "cascade attention (prefix pass + split-K + merge)" if cascade else "decode_split_kernel",
-            "split_us": split_s * 1e6, "split_kv_gbs": kv / split_s / 1e9, "split_hbm_frac": kv / split_s / 1e9 / peak}
+            "split_us": split_s * 1e6, "split_kv_gbs": kv / split_s / 1e9, "split_hbm_frac": kv / split_s / 1e9 / peak,
+            # ncu DRAM bytes of one split-kernel launch, when profiles/traffic.txt holds a capture of the
+            # current kernel source for this workload (else None)
+            "split_traffic": None if cascade else stored_traffic(w.name)}
 
 
 def per_workload_lines(args, flush_l2, peak) -> list:
