@@ -775,6 +775,21 @@ def test_maximum_group(q_len):
     full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
 
 
+def test_head_dim_256_splits_above_the_smallest():
+    """At head_dim 256 the plan targets three CTAs per SM: a sequence longer than MEMRA_SPLIT_TOKENS x
+    (SMs x 3 / KV heads) gets splits wider than the smallest, set by its length (verify rows too)."""
+    import decode_attention_block_memra_gb300 as memra
+    n_kv = 2
+    S = max(1, torch.cuda.get_device_properties(0).multi_processor_count * 3 // n_kv)
+    T = S * memra.SPLIT_TOKENS + 40_003                 # -(-T // S) passes the smallest split
+    assert -(-T // S) > memra.SPLIT_TOKENS
+    w = W.make_workload("d256_wide_splits", batch=1, q_len=2, n_heads=16, n_kv_heads=n_kv, head_dim=256,
+                        k_fmt="fp8", v_fmt="q4_0", seed=256, seq_lens=[T], permute_pages=True)
+    res = run_fused(w)
+    assert res.flags == 0
+    full_parity.check(w, res.out, res.k_pool, res.v_pool, res.initial_k_pool, res.initial_v_pool, tol=TOL)
+
+
 def test_splits_at_the_largest_split_size():
     import decode_attention_block_memra_gb300 as memra
     n_kv = 32
